@@ -33,8 +33,10 @@ def _nvcc() -> str:
 
 
 def _deps():
+    inc = os.path.join(ROOT, "include")
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(ROOT, "include", "lsr.h"))
+    files += [os.path.join(inc, f) for f in os.listdir(inc)
+              if f.endswith(".h")]
     return files
 
 
