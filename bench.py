@@ -136,6 +136,63 @@ def measured_peaks():
             "source": "fallback"}
 
 
+# Dense bf16 rate of one SM's tensor core: an M=128, N=256, K=16 tcgen05
+# product every 128 cycles (measured by the issue-rate probe summarised in
+# profiles/mma_rate.md).
+TENSOR_FLOP_PER_CLK_SM = 8192
+NOMINAL_DENSE_BF16_TFLOPS = 2250.0
+
+
+def num_sms() -> int:
+    if torch.cuda.is_available():
+        return torch.cuda.get_device_properties(0).multi_processor_count
+    return 152
+
+
+def tensor_peaks(clocks):
+    """The tensor core's dense bf16 rate (TFLOP/s) at the SM's maximum clock
+    and at the median clock sampled during the timed region."""
+    sms = num_sms()
+    mx = (clocks or {}).get("sm_max_mhz") or 2070.0
+    med = (clocks or {}).get("sm_mhz") or mx
+    rate = TENSOR_FLOP_PER_CLK_SM * sms * 1e6 / 1e12
+    return {"at_max_clock": rate * mx, "at_sampled_clock": rate * med,
+            "sms": sms, "max_mhz": mx, "sampled_mhz": med}
+
+
+def peak_pcts(value, peaks, clocks):
+    """The step's rate as a percentage of each bf16 reference: the tensor
+    core's own rate at the maximum and at the sampled clock, NVIDIA's nominal
+    dense figure, and the cuBLAS matmul rates measured on this machine (a
+    library rate: a good kernel can exceed it)."""
+    tp = tensor_peaks(clocks)
+    return {
+        "pct_tensor_peak_max_clock": 100 * value / tp["at_max_clock"],
+        "pct_tensor_peak_sampled_clock": 100 * value / tp["at_sampled_clock"],
+        "pct_nominal_dense_bf16": 100 * value / NOMINAL_DENSE_BF16_TFLOPS,
+        "pct_bf16_peak_burst": 100 * value / peaks["bf16"],
+        "pct_bf16_peak_sustained": 100 * value / peaks["bf16_sustained"],
+        "tensor_peak_tflops_max_clock": tp["at_max_clock"],
+        "tensor_peak_tflops_sampled_clock": tp["at_sampled_clock"],
+    }
+
+
+def tensor_roofline(dom, achieved, peaks, clocks, traffic):
+    """Roofline of a tensor-bound kernel: `peak`/`frac` against the measured
+    sustained cuBLAS rate, `frac_at_clock` against the tensor core's rate at
+    the sampled SM clock, `frac_max_clock` at the maximum clock."""
+    tp = tensor_peaks(clocks)
+    peak = peaks["bf16_sustained"]
+    return {"bound": "tensor", "kernel": dom, "achieved": achieved,
+            "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_kind": f"bf16 sustained cuBLAS rate ({peaks['source']})",
+            "frac_at_clock": achieved / tp["at_sampled_clock"],
+            "frac_max_clock": achieved / tp["at_max_clock"],
+            "tensor_peak_at_clock": tp["at_sampled_clock"],
+            "tensor_peak_max_clock": tp["at_max_clock"],
+            "traffic": traffic}
+
+
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -442,11 +499,9 @@ def gpu_arm(args, cfg):
         dom, n_dom, t_dom, fl_dom = "attn_fwd", n_fw, t_fw, fl["fwd"]
     per_launch_flops = fl_dom / cfg.blocks
     achieved = per_launch_flops / (t_dom / n_dom * 1e-3) / 1e12
-    peak = peaks["bf16_sustained"]
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved,
-                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_kind": f"bf16 sustained ({peaks['source']})",
-                "traffic": traffic_record(dom)}
+    clocks = clk.summary()
+    roofline = tensor_roofline(dom, achieved, peaks, clocks,
+                               traffic_record(dom))
     kernels_ms = {k: round(t / max(n, 1), 4) for k, (n, t) in kern.items()}
     per_step = {k: t / args.steps for k, (n, t) in kern.items()}
     phases = {
@@ -528,14 +583,12 @@ def gpu_arm(args, cfg):
                        "blocks": cfg.blocks, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
                        "head_dim": cfg.d, "page_size": cfg.page_size,
                        "shards": cfg.shards, "flops_per_step": total_flops,
-                       "pct_bf16_peak_burst": 100 * value / peaks["bf16"],
-                       "pct_bf16_peak_sustained":
-                           100 * value / peaks["bf16_sustained"],
+                       **peak_pcts(value, peaks, clocks),
                        "l2": l2_note(cfg),
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline, "kernel_ms_per_launch": kernels_ms,
             "phases": phases, "side_kernels": side,
-            "gpu_launches": launches, "clocks": clk.summary(),
+            "gpu_launches": launches, "clocks": clocks,
             "e2e": e2e, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -612,14 +665,11 @@ def gpu_latent_arm(args, cfg):
     else:
         dom, n_dom, t_dom, fl_dom = "attn_fwd", n_fw, t_fw, fl["fwd"]
     achieved = (fl_dom / cfg.blocks) / (t_dom / n_dom * 1e-3) / 1e12
-    peak = peaks["bf16_sustained"]
     # DRAM bytes per launch are recorded for the 2M-position latent
     # workload only (key "<kernel>_latent" in profiles/ncu_traffic.json)
     traffic = traffic_record(dom + "_latent") if cfg.name == "latent" else None
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved,
-                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_kind": f"bf16 sustained ({peaks['source']})",
-                "traffic": traffic}
+    clocks = clk.summary()
+    roofline = tensor_roofline(dom, achieved, peaks, clocks, traffic)
     kernels_ms = {k: round(t / max(n, 1), 4) for k, (n, t) in kern.items()}
 
     e2e = None
@@ -675,13 +725,11 @@ def gpu_latent_arm(args, cfg):
                        "latent_dim": cfg.d_c, "rope_dim": cfg.d_r,
                        "page_size": cfg.page_size, "shards": cfg.shards,
                        "flops_per_step": total_flops,
-                       "pct_bf16_peak_burst": 100 * value / peaks["bf16"],
-                       "pct_bf16_peak_sustained":
-                           100 * value / peaks["bf16_sustained"],
+                       **peak_pcts(value, peaks, clocks),
                        "l2": l2_note(cfg),
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline, "kernel_ms_per_launch": kernels_ms,
-            "gpu_launches": launches, "clocks": clk.summary(),
+            "gpu_launches": launches, "clocks": clocks,
             "e2e": e2e, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -777,6 +825,7 @@ def gpu_latent_group_arm(args, cfg):
     value = world * flops / (ms * 1e-3) / 1e12
     peaks = measured_peaks()
     if rank == 0:
+        clocks = clk.summary()
         print(json.dumps({
             "metric": metric_for(cfg), "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -786,10 +835,10 @@ def gpu_latent_group_arm(args, cfg):
                        "concurrent": K, "lengths": lengths, "Hq": cfg.Hq,
                        "latent_dim": cfg.d_c, "rope_dim": cfg.d_r,
                        "flops_per_group": flops,
-                       "pct_bf16_peak_burst": 100 * value / peaks["bf16"],
+                       **peak_pcts(value, peaks, clocks),
                        "step": "one group", "l2": l2_note(cfg)},
             "time_per_group_ms": ms, "peak_allocated_bytes": peak,
-            "gpu_launches": launches, "clocks": clk.summary(),
+            "gpu_launches": launches, "clocks": clocks,
         }), flush=True)
 
 
@@ -875,6 +924,7 @@ def gpu_group_arm(args, cfg):
     if rank == 0:
         peaks = measured_peaks()
         value = world * flops / (ms * 1e-3) / 1e12
+        clocks = clk.summary()
         print(json.dumps({
             "metric": metric_for(cfg), "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -884,14 +934,14 @@ def gpu_group_arm(args, cfg):
                        "lengths": lengths, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
                        "head_dim": cfg.d, "page_size": cfg.page_size,
                        "shards": cfg.shards, "flops_per_group": flops,
-                       "pct_bf16_peak_burst": 100 * value / peaks["bf16"],
+                       **peak_pcts(value, peaks, clocks),
                        "step": "one group of G serial replays",
                        "l2": l2_note(cfg)},
             "time_per_group_ms": ms,
             "peak_allocated_bytes_G2": peak2,
             "peak_allocated_bytes_G8": peak8,
             "peak_growth_G2_to_G8_bytes": peak8 - peak2,
-            "gpu_launches": launches, "clocks": clk.summary(),
+            "gpu_launches": launches, "clocks": clocks,
         }), flush=True)
 
 
@@ -974,6 +1024,7 @@ def group_concurrent(args, cfg, wl, sess, K, slot, lengths, world, rank,
     if rank == 0:
         peaks = measured_peaks()
         value = world * flops / (ms * 1e-3) / 1e12
+        clocks = clk.summary()
         print(json.dumps({
             "metric": metric_for(cfg), "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -982,12 +1033,12 @@ def group_concurrent(args, cfg, wl, sess, K, slot, lengths, world, rank,
             "config": {"workload": cfg.name, "P": cfg.P, "G": cfg.G,
                        "concurrent": K, "lengths": lengths,
                        "flops_per_group": flops,
-                       "pct_bf16_peak_burst": 100 * value / peaks["bf16"],
+                       **peak_pcts(value, peaks, clocks),
                        "step": f"one group, {len(plans)} launches of up to "
                                f"{K} responses",
                        "l2": l2_note(cfg)},
             "time_per_group_ms": ms, "peak_allocated_bytes": peak,
-            "gpu_launches": launches, "clocks": clk.summary(),
+            "gpu_launches": launches, "clocks": clocks,
         }), flush=True)
 
 

@@ -16,8 +16,11 @@
  * "Preserve gradient semantics, not just forward outputs").
  *
  * Conventions shared by every entry point.
- *  - All device memory is owned by the caller.  The library allocates no
- *    device memory; it never frees what it is given.
+ *  - All device memory is owned by the caller.  The library calls no
+ *    device allocator and never frees what it is given.  The one exception
+ *    is a fixed 64 MiB scratch array in the library's own device memory,
+ *    used only by lsr_replay_attn_bwd_noalloc and held by every GPU that
+ *    loads the library until the process exits.
  *  - bf16 means IEEE bfloat16 stored as 2 bytes; fp32 is IEEE float.
  *  - Every device pointer must be 16-byte aligned.  Tensors are dense and
  *    row-major in the index order written next to them.
@@ -347,6 +350,21 @@ lsr_status lsr_score_fwd(lsr_pool_t pool, const void* q, int Hq, int R_b,
  */
 lsr_status lsr_selftest_bounded_wait(int* dev_status, int limit_us,
                                      void* stream);
+
+/*
+ * lsr_pool_set_wait_limit -- limit of the attention kernels' pipeline waits
+ * for every later call on this pool (either kind).  The pages describe no
+ * such call.  Each pipeline role (copy producer, MMA issuer, softmax and dS
+ * warps) waits for the others on mbarriers; a wait that runs past the limit
+ * makes the whole CTA give up: it sets LSR_DEV_WAIT_TIMEOUT in the pool's
+ * status word, lets its issued copies and products finish, frees its tensor
+ * memory and exits, leaving the outputs of that call undefined and the
+ * context usable.  limit_us: 1 .. 4000000 microseconds, or 0 for the
+ * default of 4 s.  A limit of a few microseconds makes waits run out on
+ * purpose, which is how the abort path is tested.  Host-side only; takes
+ * effect from the next launch.
+ */
+lsr_status lsr_pool_set_wait_limit(lsr_pool_t pool, int limit_us);
 
 /*
  * lsr_pool_device_status -- synchronise `stream`, then copy the pool's

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(192, 1)
         const int row = pool_row(p, kr.page0, (rev ? n_tiles - 1 - j : j) * BN, g);
         const int ks = j % KST, vs = j % VST;
         if (j >= KST &&
-            !warp_wait(&s.k_empty[ks], ((j / KST) & 1) ^ 1, &s.abort_flag))
+            !warp_wait(&s.k_empty[ks], ((j / KST) & 1) ^ 1, &s.abort_flag, p.wait_ns))
           break;
         mbar_expect_tx_e(&s.k_full[ks], C::KV_BYTES);
 #pragma unroll
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_2d_e(s.k[ks] + c * BN * 64, &mk, &s.k_full[ks], c * 64, row);
         k_issued = j + 1;
         if (j >= VST &&
-            !warp_wait(&s.v_empty[vs], ((j / VST) & 1) ^ 1, &s.abort_flag))
+            !warp_wait(&s.v_empty[vs], ((j / VST) & 1) ^ 1, &s.abort_flag, p.wait_ns))
           break;
         mbar_expect_tx_e(&s.v_full[vs], C::KV_BYTES);
 #pragma unroll
@@ -149,25 +149,24 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_2d_e(s.v[vs] + c * BN * 64, &mv, &s.v_full[vs], c * 64, row);
         v_issued = j + 1;
       }
-      if (s.abort_flag) {
-        mbar_wait_drain(&s.qd_full, 0);
-        for (int t = max(0, k_issued - KST); t < k_issued; ++t)
-          mbar_wait_drain(&s.k_full[t % KST], (t / KST) & 1);
-        for (int t = max(0, v_issued - VST); t < v_issued; ++t)
-          mbar_wait_drain(&s.v_full[t % VST], (t / VST) & 1);
-      }
+      // every copy lands before the CTA can exit (see the forward kernel)
+      mbar_wait_drain(&s.qd_full, 0);
+      for (int t = max(0, k_issued - KST); t < k_issued; ++t)
+        mbar_wait_drain(&s.k_full[t % KST], (t / KST) & 1);
+      for (int t = max(0, v_issued - VST); t < v_issued; ++t)
+        mbar_wait_drain(&s.v_full[t % VST], (t / VST) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (n_tiles > 0) {  // the whole warp: one elected lane issues
-      bool ok = warp_wait(&s.qd_full, 0, &s.abort_flag);
+      bool ok = warp_wait(&s.qd_full, 0, &s.abort_flag, p.wait_ns);
       // descriptors: one per operand tile, k-steps added as constants
       const uint64_t qd = sdesc(smem_u32(s.q), 16, 1024);
       const uint64_t dd = sdesc(smem_u32(s.dO), 16, 1024);
       for (int j = 0; ok && j <= n_tiles; ++j) {
         if (j < n_tiles) {
           const int ks = j % KST, vs = j % VST, b = j & 1;
-          if (!warp_wait(&s.k_full[ks], (j / KST) & 1, &s.abort_flag)) break;
+          if (!warp_wait(&s.k_full[ks], (j / KST) & 1, &s.abort_flag, p.wait_ns)) break;
           tc_fence_after();
           const uint64_t kd = sdesc(smem_u32(s.k[ks]), 16, 1024);
           const uint64_t vd = sdesc(smem_u32(s.v[vs]), 16, 1024);
@@ -176,9 +175,9 @@ __global__ void __launch_bounds__(192, 1)
             mma_ss_e(tm + b * BN, qd + kmaj_step<kTileRows>(k),
                      kd + kmaj_step<BN>(k), C::ID_S, k > 0);
           mma_commit_e(&s.s_full[b]);
-          if (j >= 1 && !warp_wait(&s.dp_free, (j - 1) & 1, &s.abort_flag))
+          if (j >= 1 && !warp_wait(&s.dp_free, (j - 1) & 1, &s.abort_flag, p.wait_ns))
             break;
-          if (!warp_wait(&s.v_full[vs], (j / VST) & 1, &s.abort_flag)) break;
+          if (!warp_wait(&s.v_full[vs], (j / VST) & 1, &s.abort_flag, p.wait_ns)) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
@@ -189,7 +188,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (j >= 1) {
           const int i = j - 1, ks = i % KST, b = i & 1;
-          if (!warp_wait(&s.ds_full[b], (i >> 1) & 1, &s.abort_flag)) break;
+          if (!warp_wait(&s.ds_full[b], (i >> 1) & 1, &s.abort_flag, p.wait_ns)) break;
           tc_fence_after();
           // K as the MN-major B operand: 16 key rows of 128 bytes per step
           const uint64_t kd = sdesc(smem_u32(s.k[ks]), BN * 128, 1024);
@@ -219,7 +218,7 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j & 1;
-      if (!warp_wait(&s.dp_full, j & 1, &s.abort_flag)) {
+      if (!warp_wait(&s.dp_full, j & 1, &s.abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -231,7 +230,7 @@ __global__ void __launch_bounds__(192, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&s.dp_free);
-      if (!warp_wait(&s.s_full[b], (j >> 1) & 1, &s.abort_flag)) {
+      if (!warp_wait(&s.s_full[b], (j >> 1) & 1, &s.abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -257,7 +256,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     float* drow = p.o + (((size_t)part * p.R_b + r) * p.Hq + h) * D;
     if (ok && n_tiles > 0) {
-      ok = warp_wait(&s.dq_ready, 0, &s.abort_flag);
+      ok = warp_wait(&s.dq_ready, 0, &s.abort_flag, p.wait_ns);
       tc_fence_after();
       if (ok) {
 #pragma unroll
@@ -395,7 +394,7 @@ __global__ void __launch_bounds__(192, 1)
     for (int i = 0; i < n_q; ++i) {
       const int st = i % ST;
       if (i >= ST &&
-          !warp_wait(&s.q_empty[st], ((i / ST) & 1) ^ 1, &s.abort_flag))
+          !warp_wait(&s.q_empty[st], ((i / ST) & 1) ^ 1, &s.abort_flag, p.wait_ns))
         break;
       const int qt = qt0 + i;
       const int r0 = qt * p.rows_per_tile;
@@ -421,18 +420,18 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(&s.q_full[st]);
       issued = i + 1;
     }
-    if (lane == 0 && s.abort_flag) {
+    if (lane == 0) {  // every copy lands before the CTA can exit
       mbar_wait_drain(&s.kv_full, 0);
       for (int t = max(0, issued - ST); t < issued; ++t)
         mbar_wait_drain(&s.q_full[t % ST], (t / ST) & 1);
     }
   } else if (warp == 1) {
     {  // the whole warp: one elected lane issues
-      bool ok = warp_wait(&s.kv_full, 0, &s.abort_flag);
+      bool ok = warp_wait(&s.kv_full, 0, &s.abort_flag, p.wait_ns);
       const uint32_t ka = smem_u32(s.k), va = smem_u32(s.v);
       for (int i = 0; ok && i < n_q; ++i) {
         const int st = i % ST;
-        if (!warp_wait(&s.q_full[st], (i / ST) & 1, &s.abort_flag)) break;
+        if (!warp_wait(&s.q_full[st], (i / ST) & 1, &s.abort_flag, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t qa = smem_u32(s.q[st]), da = smem_u32(s.dO[st]);
 #pragma unroll
@@ -446,7 +445,7 @@ __global__ void __launch_bounds__(192, 1)
                    sdesc(da, 16, 1024) + kmaj_step<128>(k), C::ID_T, k > 0);
         }
         mma_commit_e(&s.s_full);
-        if (!warp_wait(&s.p_full, i & 1, &s.abort_flag)) break;
+        if (!warp_wait(&s.p_full, i & 1, &s.abort_flag, p.wait_ns)) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k) {
@@ -474,7 +473,7 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
       const int st = i % ST;
-      if (!warp_wait(&s.s_full, i & 1, &s.abort_flag)) {
+      if (!warp_wait(&s.s_full, i & 1, &s.abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -511,7 +510,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(&s.p_full);
     }
     if (ok) {
-      ok = warp_wait(&s.acc_ready, 0, &s.abort_flag);
+      ok = warp_wait(&s.acc_ready, 0, &s.abort_flag, p.wait_ns);
       tc_fence_after();
     }
     if (ok && n_q > 0) {

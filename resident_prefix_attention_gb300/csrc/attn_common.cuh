@@ -25,6 +25,7 @@ struct AttnParams {
   float scale;           // softmax scale
   float scale_log2;      // scale * log2(e)
   int num_sms;           // CTAs resident at once (one per SM)
+  uint64_t wait_ns;      // limit of every pipeline wait (drains excepted)
   RespTable resp;        // which response each row of q belongs to
 };
 
@@ -120,8 +121,9 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar,
 
 // Warp-uniform bounded wait: every lane waits, the warp agrees on success.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag) {
-  bool ok = mbar_wait(bar, parity, abort_flag);
+                                          volatile int* abort_flag,
+                                          uint64_t limit_ns) {
+  bool ok = mbar_wait(bar, parity, abort_flag, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -181,6 +183,7 @@ inline AttnParams make_params(const Pool& pl, const BlockGeom& g,
   p.scale = g.scale;
   p.scale_log2 = g.scale * kLog2e;
   p.num_sms = num_sms();
+  p.wait_ns = pl.wait_ns;
   return p;
 }
 

@@ -9,13 +9,14 @@
 // explainer ("Two incompatible architectures, same transaction", Qwen
 // bullet) composes into the exact output.
 //
-// Warp roles (320 threads): warp 0 issues TMA loads (both Q tiles once, then
-// K and V pages through the page table into one ring, in the order K_0,
-// V_0, K_1, ...), warp 1
-// allocates TMEM and issues tcgen05.mma (the whole warp runs the issue loop,
-// an elected lane issues), warps 2-5 and 6-9 are
-// the softmax warpgroups of query tiles 0 and 1 (warp w owns TMEM lanes
-// 32*(w%4) .. +31).  The MMA order S0_j, S1_j, PV0_j, S0_j+1, PV1_j, S1_j+1,
+// Warp roles (384 threads, three warpgroups): warp 0 issues TMA loads (both
+// Q tiles once, then K and V pages through the page table into one ring, in
+// the order K_0, V_0, K_1, ...), warp 1 allocates TMEM and issues
+// tcgen05.mma (the whole warp runs the issue loop, an elected lane issues),
+// warps 2-3 idle; warps 4-7 and 8-11 are the softmax warpgroups of query
+// tiles 0 and 1 (warp w owns TMEM lanes 32*(w%4) .. +31).  The first
+// warpgroup hands registers to the softmax warpgroups (setmaxnreg), which
+// hold a whole 128-key row of S in registers.  The MMA order S0_j, S1_j, PV0_j, S0_j+1, PV1_j, S1_j+1,
 // ... keeps one tile's products queued while the other tile's softmax runs,
 // and each K/V tile in shared memory serves both query tiles.
 //
@@ -48,7 +49,17 @@ struct FwdCfg {
   static constexpr uint32_t TMEM_COLS = (2 * BN + 2 * DV <= 256) ? 256 : 512;
   static constexpr uint32_t ID_S = idesc_bf16(128, BN, false, false);
   static constexpr uint32_t ID_PV = idesc_bf16(128, DV, false, true);
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 384;
+  // Registers per thread: the block launches at kLaunchRegs (the cap for
+  // 384 threads); the first warpgroup drops to kRegsIssue and the two
+  // softmax warpgroups rise to kRegsSoftmax, which adds up to the launch
+  // total exactly.
+  static constexpr int kLaunchRegs = 168;
+  static constexpr int kRegsIssue = 120;
+  static constexpr int kRegsSoftmax = 192;
+  static_assert(128 * kRegsIssue + 256 * kRegsSoftmax <=
+                    THREADS * kLaunchRegs,
+                "register shares exceed the block's launch total");
   static_assert(2 * BN + 2 * DV <= 512, "TMEM holds two S and two O tiles");
   static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= DQK, "box widths");
   static_assert(LAT || DV == DQK, "K and V tiles share the ring slots");
@@ -97,33 +108,27 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem,
 
 // One pass of the softmax over a row of S (x: the raw logits, masked keys at
 // -inf): P = 2^(x * scale_log2 - mu) in packed pairs, written as bf16 into
-// the BN/2 TMEM columns that start at tmem_s, with the sum of P
-// as computed (s_exact, for lse) and of the bf16 P the product sees (s_rnd,
-// for normalising O).  With TRACK_MAX it also returns the row's max of x,
-// in independent three-input chains that ride along the exponentials.
-template <int BN, bool TRACK_MAX>
+// the BN/2 TMEM columns that start at tmem_s, with the sum of P as computed
+// (s_exact, for lse) and of the bf16 P the product sees (s_rnd, for
+// normalising O).  Per pair of keys the pass issues one packed FMA, two
+// exponentials, one packed conversion, one packed add and two adds of a
+// bf16 half into fp32.
+template <int BN>
 __device__ __forceinline__ void p_pass(const float (&x)[BN], float scale_log2,
                                        float mu, uint32_t tmem_s,
-                                       float& s_exact, float& s_rnd,
-                                       float& xmax) {
+                                       float& s_exact, float& s_rnd) {
   const uint64_t sc2 = f32x2(scale_log2, scale_log2);
   const uint64_t nm2 = f32x2(-mu, -mu);
-  // all of x stays live for a possible second pass, so the pass itself
-  // keeps few registers: P goes out every 16 packed columns, two partial
-  // sums of each kind and four max chains
+  // P goes out every 16 packed columns; two partial sums of each kind keep
+  // the add chains short
   uint64_t r2[2] = {0ull, 0ull};
   float qa[2] = {0.f, 0.f}, qb[2] = {0.f, 0.f};
-  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int qq = 0; qq < BN / 32; ++qq) {
     uint32_t pk[16];
 #pragma unroll
     for (int c = 0; c < 32; c += 2) {
       const int cc = qq * 32 + c;
-      if (TRACK_MAX) {
-        const int m = (c >> 1) & 3;
-        m4[m] = max3f(m4[m], x[cc], x[cc + 1]);
-      }
       float t0, t1;
       f32x2_split(fma_f32x2(f32x2(x[cc], x[cc + 1]), sc2, nm2), t0, t1);
       const float p0 = ex2_approx(t0);
@@ -141,11 +146,20 @@ __device__ __forceinline__ void p_pass(const float (&x)[BN], float scale_log2,
   f32x2_split(add_f32x2(r2[0], r2[1]), s0, s1);
   s_exact = s0 + s1;
   s_rnd = (qa[0] + qb[0]) + (qa[1] + qb[1]);
-  if (TRACK_MAX) xmax = fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
+}
+
+// Largest raw logit of a row of S, in independent three-input chains.
+template <int BN>
+__device__ __forceinline__ float row_max(const float (&x)[BN]) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < BN; c += 2)
+    m4[(c >> 1) & 3] = max3f(m4[(c >> 1) & 3], x[c], x[c + 1]);
+  return fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
 }
 
 template <int DQK, int DV, int BN, bool LAT>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq,
                     const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv,
@@ -196,6 +210,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    regs_dec<C::kRegsIssue>();
     if (n_tiles > 0) {  // the whole warp: one elected lane issues
       if (lane == 0) {
         prefetch_tmap(&mq);
@@ -215,7 +230,7 @@ __global__ void __launch_bounds__(320, 1)
         const int row = pool_row(p, kr.page0, (rev ? n_tiles - 1 - j : j) * BN, g);
         const int tk = ring_k<LAT>(j), sk = tk % NS;
         if (tk >= NS &&
-            !warp_wait(&s.empty[sk], ((tk / NS) & 1) ^ 1, &s.abort_flag))
+            !warp_wait(&s.empty[sk], ((tk / NS) & 1) ^ 1, &s.abort_flag, p.wait_ns))
           break;
         mbar_expect_tx_e(&s.full[sk], C::K_BYTES);
 #pragma unroll
@@ -226,7 +241,7 @@ __global__ void __launch_bounds__(320, 1)
         if (LAT) continue;
         const int tv = ring_v<LAT>(j), sv = tv % NS;
         if (tv >= NS &&
-            !warp_wait(&s.empty[sv], ((tv / NS) & 1) ^ 1, &s.abort_flag))
+            !warp_wait(&s.empty[sv], ((tv / NS) & 1) ^ 1, &s.abort_flag, p.wait_ns))
           break;
         mbar_expect_tx_e(&s.full[sv], C::V_BYTES);
 #pragma unroll
@@ -235,19 +250,22 @@ __global__ void __launch_bounds__(320, 1)
                         row);
         issued = tv + 1;
       }
-      if (s.abort_flag) {
-        mbar_wait_drain(&s.q_full, 0);
-        for (int t = max(0, issued - NS); t < issued; ++t)
-          mbar_wait_drain(&s.full[t % NS], (t / NS) & 1);
-      }
+      // Every copy lands before the CTA can exit.  After a normal run the
+      // consumers have already waited for all of them; after an abort
+      // (any role's wait ran out) this keeps late copies out of the shared
+      // memory of whatever CTA runs next on the SM.
+      mbar_wait_drain(&s.q_full, 0);
+      for (int t = max(0, issued - NS); t < issued; ++t)
+        mbar_wait_drain(&s.full[t % NS], (t / NS) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    regs_dec<C::kRegsIssue>();
     if (n_tiles > 0) {  // the whole warp: one elected lane issues
       const uint64_t qd0 = sdesc(smem_u32(s.q[0]), 16, 1024);
       const uint64_t qd1 = sdesc(smem_u32(s.q[1]), 16, 1024);
-      bool ok = warp_wait(&s.q_full, 0, &s.abort_flag) &&
-                warp_wait(&s.full[0], 0, &s.abort_flag);
+      bool ok = warp_wait(&s.q_full, 0, &s.abort_flag, p.wait_ns) &&
+                warp_wait(&s.full[0], 0, &s.abort_flag, p.wait_ns);
       if (ok) {
         tc_fence_after();
         const uint64_t kd = sdesc(smem_u32(s.ring[0]), 16, 1024);
@@ -262,22 +280,22 @@ __global__ void __launch_bounds__(320, 1)
         const int tv = ring_v<LAT>(j), sv = tv % NS;
         const int tk1 = ring_k<LAT>(j + 1), sk1 = tk1 % NS;
         // O0 += P0 V_j, then S0 of the next key tile over P0's columns
-        if (!warp_wait(&s.p_full[0], j & 1, &s.abort_flag)) break;
-        if (!LAT && !warp_wait(&s.full[sv], (tv / NS) & 1, &s.abort_flag))
+        if (!warp_wait(&s.p_full[0], j & 1, &s.abort_flag, p.wait_ns)) break;
+        if (!LAT && !warp_wait(&s.full[sv], (tv / NS) & 1, &s.abort_flag, p.wait_ns))
           break;
         tc_fence_after();
         const uint64_t vd = sdesc(smem_u32(s.ring[sv]), BN * 128, 1024);
         issue_pv<BN, C::ID_PV>(tm + C::TM_O, tm + BN / 2, vd, j == 0);
         mma_commit_e(&s.o_ready[0]);
         if (more) {
-          if (!warp_wait(&s.full[sk1], (tk1 / NS) & 1, &s.abort_flag)) break;
+          if (!warp_wait(&s.full[sk1], (tk1 / NS) & 1, &s.abort_flag, p.wait_ns)) break;
           tc_fence_after();
           issue_s<DQK, BN, C::ID_S>(tm, qd0,
                                     sdesc(smem_u32(s.ring[sk1]), 16, 1024));
           mma_commit_e(&s.s_full[0]);
         }
         // O1 += P1 V_j, then S1 of the next key tile
-        if (!warp_wait(&s.p_full[1], j & 1, &s.abort_flag)) break;
+        if (!warp_wait(&s.p_full[1], j & 1, &s.abort_flag, p.wait_ns)) break;
         tc_fence_after();
         issue_pv<BN, C::ID_PV>(tm + C::TM_O + DV, tm + BN + BN / 2, vd,
                                j == 0);
@@ -297,9 +315,12 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit_e(&s.mma_done);
       mbar_wait_drain(&s.mma_done, 0);
     }
+  } else if (warp < 4) {
+    regs_dec<C::kRegsIssue>();  // idle warps of the first warpgroup
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 2) >> 2;           // query tile of this warpgroup
+    regs_inc<C::kRegsSoftmax>();
+    const int t = (warp - 4) >> 2;           // query tile of this warpgroup
     const int quarter = warp & 3;
     const int mrow = quarter * 32 + lane;
     const int r = r0 + t * p.rows_per_tile + mrow / p.G;
@@ -309,18 +330,21 @@ __global__ void __launch_bounds__(320, 1)
     const int qpos = (valid && kr.causal) ? ri.qpos : INT_MAX;
     const uint32_t lane_base = tm + ((uint32_t)(quarter * 32) << 16);
     const uint32_t s_col = t * BN, o_col = C::TM_O + t * DV;
-    // mt: running row max of the scaled logits (log2 units).  mu: the
-    // reference the current P, l and O are taken against; it is raised only
-    // when the max grows by more than 2^8, so P stays <= 256 and O is
-    // rescaled rarely.  Every value uses the same mu, so the result is the
-    // same as with mu = mt.
-    // lsum: sum of P as computed (gives lse); lrnd: sum of the bf16 P the
-    // product uses (normalises O, so every key weighs the same in the
-    // numerator and the denominator)
-    float mt = -INFINITY, mu = -INFINITY, lsum = 0.f, lrnd = 0.f;
+    // mu: the reference (log2 units) that P, lsum and O are taken against:
+    // the scaled logit of the largest key seen when it was last set, rounded
+    // up to an integer.  A tile whose sum of P exceeds 2^8 (which every tile
+    // with a key more than 2^8 times the reference's weight does, and the
+    // first tile, where mu = -inf, does through inf) sets it again from the
+    // tile's max and computes P a second time; otherwise mu stays, so mu
+    // lies at most 8 below the row max (and at most 1 above it) and every P
+    // is at most 2^8.  lsum: sum of P as computed (gives
+    // lse); lrnd: sum of the bf16 P the product uses (normalises O, so every
+    // key weighs the same in the numerator and the denominator, and a row
+    // dominated by one key returns that key's V whatever its P rounds to).
+    float mu = -INFINITY, lsum = 0.f, lrnd = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      if (!warp_wait(&s.s_full[t], j & 1, &s.abort_flag)) {
+      if (!warp_wait(&s.s_full[t], j & 1, &s.abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -336,26 +360,15 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < BN; ++c)
           if (kbase + c > qpos) x[c] = -INFINITY;
       }
-      // P against the current reference first; the tile's max comes out of
-      // the same pass.  Only when it shows that the reference must be raised
-      // (always on the first tile, where mu is -inf) is P computed again
-      // against the raised one.
-      // P goes over the second half of S's columns (the PV product reads it
-      // there), so S of the first BN/2 keys survives for a second pass
-      float ls_t, lr_t, xmax;
-      p_pass<BN, true>(x, p.scale_log2, mu, lane_base + s_col + BN / 2, ls_t,
-                       lr_t, xmax);
-      mt = fmaxf(mt, xmax * p.scale_log2);
-      const bool rescale = __any_sync(0xffffffffu, mt > mu + 8.f);
+      // P against the current reference.  P goes over the second half of
+      // S's columns (the PV product reads it there), so S of the first BN/2
+      // keys survives for a second pass.
+      float ls_t, lr_t;
+      p_pass<BN>(x, p.scale_log2, mu, lane_base + s_col + BN / 2, ls_t,
+                 lr_t);
+      const bool rescale = __any_sync(0xffffffffu, !(ls_t <= 256.f));
       float alpha = 1.f;
       if (rescale) {
-        // an integer reference: rescales are exact powers of two, and P's
-        // mantissa does not depend on when the reference was raised
-        const float mu_new = fmaxf(mu, ceilf(mt));
-        alpha = ex2_approx(mu - mu_new);
-        mu = mu_new;
-        lsum *= alpha;
-        lrnd *= alpha;
         tmem_st_wait();  // the first pass's stores land before the second's
         float y[BN];
 #pragma unroll
@@ -367,15 +380,25 @@ __global__ void __launch_bounds__(320, 1)
           if (kbase + c > qpos) y[c] = -INFINITY;
 #pragma unroll
         for (int c = BN / 2; c < BN; ++c) y[c] = x[c];
-        p_pass<BN, false>(y, p.scale_log2, mu, lane_base + s_col + BN / 2,
-                          ls_t, lr_t, xmax);
+        // an integer reference: rescales are exact powers of two, and P's
+        // mantissa does not depend on when the reference was raised (so the
+        // result does not depend on the order the key tiles are walked in)
+        const float mu_new = fmaxf(mu, ceilf(row_max<BN>(y) * p.scale_log2));
+        if (mu_new != mu) {
+          alpha = ex2_approx(mu - mu_new);
+          mu = mu_new;
+          lsum *= alpha;
+          lrnd *= alpha;
+        }
+        p_pass<BN>(y, p.scale_log2, mu, lane_base + s_col + BN / 2, ls_t,
+                   lr_t);
       }
       lsum += ls_t;
       lrnd += lr_t;
       if (j > 0 && rescale) {
         // S_t of this tile was issued after PV_t of the previous one, so
         // that product is already complete; the wait documents it.
-        if (!warp_wait(&s.o_ready[t], (j - 1) & 1, &s.abort_flag)) {
+        if (!warp_wait(&s.o_ready[t], (j - 1) & 1, &s.abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -395,8 +418,9 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(&s.p_full[t]);
     }
+    tmem_st_wait();  // an aborted tile's stores complete before TMEM is freed
     if (ok && n_tiles > 0) {
-      ok = warp_wait(&s.o_final, 0, &s.abort_flag);
+      ok = warp_wait(&s.o_final, 0, &s.abort_flag, p.wait_ns);
       tc_fence_after();
       if (ok) {
         const float inv = 1.f / lrnd;
@@ -418,10 +442,11 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         if (valid) {
-          // report l against the true row max
+          // (m, l): the reference in natural-log units and the sum of
+          // exp(logit - m) against it
           const size_t si = ((size_t)part * p.Hq + h) * p.R_b + r;
-          p.m[si] = mt * kLn2;
-          p.l[si] = lsum * ex2_approx(mu - mt);
+          p.m[si] = mu * kLn2;
+          p.l[si] = lsum;
         }
       }
     } else if (n_tiles == 0 && valid) {
@@ -483,6 +508,7 @@ cudaError_t launch_attn_fwd(const Pool& pl, const BlockGeom& g,
   p.scale = g.scale;
   p.scale_log2 = g.scale * kLog2e;
   p.num_sms = num_sms();
+  p.wait_ns = pl.wait_ns;
   const int n_pairs = (g.n_qtiles + 1) / 2;
   const int grid = n_pairs * g.Hkv * (g.num_shards + 1);
   if (pl.latent) {

@@ -11,6 +11,9 @@ namespace lsr {
 // times the G query heads that share one kv head.
 constexpr int kTileRows = 128;
 
+// Default limit of an in-kernel pipeline wait: 4 s.
+constexpr uint64_t kDefaultWaitNs = 4000000000ull;
+
 // A K/V pool holds [num_pages][Hkv][page_size][head_dim] K and V pages.  A
 // latent pool holds one row [c, r] of width head_dim per position
 // ([num_pages][1][page_size][head_dim]); it is the key, and its first v_dim
@@ -22,6 +25,8 @@ struct Pool {
   int* dev_status;
   int v_dim;    // value width: head_dim for K/V pools, d_c for latent pools
   bool latent;
+  // limit of the attention kernels' pipeline waits (lsr_pool_set_wait_limit)
+  uint64_t wait_ns = kDefaultWaitNs;
 };
 
 // Query blocks of one or more responses stacked along the rows of q.

@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(192, 1)
             pool_row(p, kr.page0, (rev ? n_tiles - 1 - j : j) * BN, g);
         const int ks = j % KST;
         if (j >= KST &&
-            !warp_wait(&s.k_empty[ks], ((j / KST) & 1) ^ 1, &s.abort_flag))
+            !warp_wait(&s.k_empty[ks], ((j / KST) & 1) ^ 1, &s.abort_flag, p.wait_ns))
           break;
         mbar_expect_tx_e(&s.k_full[ks], C::K_BYTES);
 #pragma unroll
@@ -147,24 +147,23 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_2d_e(s.k[ks] + c * BN * 64, &mk, &s.k_full[ks], c * 64, row);
         issued = j + 1;
       }
-      if (s.abort_flag) {
-        mbar_wait_drain(&s.qd_full, 0);
-        for (int t = max(0, issued - KST); t < issued; ++t)
-          mbar_wait_drain(&s.k_full[t % KST], (t / KST) & 1);
-      }
+      // every copy lands before the CTA can exit
+      mbar_wait_drain(&s.qd_full, 0);
+      for (int t = max(0, issued - KST); t < issued; ++t)
+        mbar_wait_drain(&s.k_full[t % KST], (t / KST) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (n_tiles > 0) {  // the whole warp: one elected lane issues
-      bool ok = warp_wait(&s.qd_full, 0, &s.abort_flag);
+      bool ok = warp_wait(&s.qd_full, 0, &s.abort_flag, p.wait_ns);
       const uint32_t qa = smem_u32(s.q), da = smem_u32(s.dO);
       for (int j = 0; ok && j <= n_tiles; ++j) {
         uint32_t ka = 0;
         if (j < n_tiles) {
           const int ks = j % KST;
-          if (!warp_wait(&s.k_full[ks], (j / KST) & 1, &s.abort_flag)) break;
+          if (!warp_wait(&s.k_full[ks], (j / KST) & 1, &s.abort_flag, p.wait_ns)) break;
           // S columns free: the dS warps hold S_{j-1} in registers
-          if (j >= 1 && !warp_wait(&s.s_free, (j - 1) & 1, &s.abort_flag))
+          if (j >= 1 && !warp_wait(&s.s_free, (j - 1) & 1, &s.abort_flag, p.wait_ns))
             break;
           tc_fence_after();
           ka = smem_u32(s.k[ks]);
@@ -180,7 +179,7 @@ __global__ void __launch_bounds__(192, 1)
           // dq~ += dS_{j-1} L_{j-1}; dS_{j-1} complete also means dP_{j-1}
           // has been read, so dP_j may follow
           const int i = j - 1, ksi = i % KST;
-          if (!warp_wait(&s.ds_full, i & 1, &s.abort_flag)) break;
+          if (!warp_wait(&s.ds_full, i & 1, &s.abort_flag, p.wait_ns)) break;
           tc_fence_after();
           const uint32_t kai = smem_u32(s.k[ksi]);
 #pragma unroll
@@ -219,7 +218,7 @@ __global__ void __launch_bounds__(192, 1)
     const float Dv = valid ? p.Dvec[(size_t)h * p.R_b + r] : 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      if (!warp_wait(&s.s_full, j & 1, &s.abort_flag)) {
+      if (!warp_wait(&s.s_full, j & 1, &s.abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -230,7 +229,7 @@ __global__ void __launch_bounds__(192, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&s.s_free);
-      if (!warp_wait(&s.dp_full, j & 1, &s.abort_flag)) {
+      if (!warp_wait(&s.dp_full, j & 1, &s.abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -256,7 +255,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     float* drow = p.o + (((size_t)part * p.R_b + r) * p.Hq + h) * kDL;
     if (ok && n_tiles > 0) {
-      ok = warp_wait(&s.dq_ready, 0, &s.abort_flag);
+      ok = warp_wait(&s.dq_ready, 0, &s.abort_flag, p.wait_ns);
       tc_fence_after();
       if (ok) {
 #pragma unroll
@@ -382,7 +381,7 @@ __global__ void __launch_bounds__(192, 1)
     for (int i = 0; i < n_q; ++i) {
       const int st = i % ST;
       if (i >= ST &&
-          !warp_wait(&s.q_empty[st], ((i / ST) & 1) ^ 1, &s.abort_flag))
+          !warp_wait(&s.q_empty[st], ((i / ST) & 1) ^ 1, &s.abort_flag, p.wait_ns))
         break;
       const int r0 = (qt0 + i) * p.rows_per_tile;
       if (lane == 0) {
@@ -408,18 +407,18 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(&s.q_full[st]);
       issued = i + 1;
     }
-    if (lane == 0 && s.abort_flag) {
+    if (lane == 0) {  // every copy lands before the CTA can exit
       mbar_wait_drain(&s.kv_full, 0);
       for (int t = max(0, issued - ST); t < issued; ++t)
         mbar_wait_drain(&s.q_full[t % ST], (t / ST) & 1);
     }
   } else if (warp == 1) {
     {  // the whole warp: one elected lane issues
-      bool ok = warp_wait(&s.kv_full, 0, &s.abort_flag);
+      bool ok = warp_wait(&s.kv_full, 0, &s.abort_flag, p.wait_ns);
       const uint32_t ka = smem_u32(s.k);
       for (int i = 0; ok && i < n_q; ++i) {
         const int st = i % ST;
-        if (!warp_wait(&s.q_full[st], (i / ST) & 1, &s.abort_flag)) break;
+        if (!warp_wait(&s.q_full[st], (i / ST) & 1, &s.abort_flag, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t qa = smem_u32(s.q[st]), da = smem_u32(s.dO[st]);
         // S^T = L q~^T (keys on the lanes, query rows as N)
@@ -435,7 +434,7 @@ __global__ void __launch_bounds__(192, 1)
                    sdesc(da, 16, 1024) + kmaj_step<128>(k), C::ID_T, k > 0);
         }
         mma_commit_e(&s.s_full);
-        if (!warp_wait(&s.p_full, i & 1, &s.abort_flag)) break;
+        if (!warp_wait(&s.p_full, i & 1, &s.abort_flag, p.wait_ns)) break;
         tc_fence_after();
         // dL += (scale dS^T) q~ over all kDL columns (first product
         // initialises the accumulator) ...
@@ -464,7 +463,7 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
       const int st = i % ST;
-      if (!warp_wait(&s.s_full, i & 1, &s.abort_flag)) {
+      if (!warp_wait(&s.s_full, i & 1, &s.abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -505,7 +504,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(&s.p_full);
     }
     if (ok) {
-      ok = warp_wait(&s.acc_ready, 0, &s.abort_flag);
+      ok = warp_wait(&s.acc_ready, 0, &s.abort_flag, p.wait_ns);
       tc_fence_after();
     }
     if (ok && n_q > 0) {

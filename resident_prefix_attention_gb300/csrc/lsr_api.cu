@@ -279,6 +279,15 @@ lsr_status lsr_page_pool_create(int num_pages, int page_size, int num_kv_heads,
   return LSR_OK;
 }
 
+lsr_status lsr_pool_set_wait_limit(lsr_pool_t pool, int limit_us) {
+  LSR_REQUIRE(pool != nullptr, "pool is NULL");
+  LSR_REQUIRE(limit_us >= 0 && limit_us <= 4000000,
+              "limit_us (%d) must be 0 (default) or 1 .. 4000000", limit_us);
+  pool->p.wait_ns =
+      limit_us == 0 ? kDefaultWaitNs : (uint64_t)limit_us * 1000ull;
+  return LSR_OK;
+}
+
 lsr_status lsr_page_pool_destroy(lsr_pool_t pool) {
   delete pool;
   return LSR_OK;

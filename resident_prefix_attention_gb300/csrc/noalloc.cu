@@ -60,13 +60,15 @@ extern "C" lsr_status lsr_replay_attn_bwd_noalloc(
     const float* lse, int Hq, int R_b, int P, int resp_pos0,
     const int32_t* page_table, int table_len, int num_shards, float scale,
     float* dq, float* dk_resp, float* dv_resp, void* stream) {
-  if (pool == nullptr) {
-    lsr::set_error("pool is NULL");
-    return LSR_ERR_INVALID_ARG;
-  }
+  // The block's geometry is checked first, as lsr_replay_attn_bwd checks
+  // it, so that a bad argument is reported as itself and not as a scratch
+  // size problem.
+  lsr::BlockGeom g;
+  lsr_status st = lsr::block_geom(pool, Hq, R_b, P, resp_pos0, table_len,
+                                  num_shards, scale, false, &g);
+  if (st != LSR_OK) return st;
   size_t need = 0;
-  lsr_status st =
-      lsr_bwd_workspace_size(num_shards, Hq, R_b, pool->p.head_dim, &need);
+  st = lsr_bwd_workspace_size(num_shards, Hq, R_b, g.d, &need);
   if (st != LSR_OK) return st;
   if (need > kScratchBytes) {
     lsr::set_error(

@@ -52,17 +52,37 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Non-blocking test of a phase (mbarrier.try_wait may suspend the thread
+// for a while before it returns false; test_wait returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar,
+                                               uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: returns false after ~limit_ns without the phase completing.
 // `abort_flag` (shared) lets one timed-out role stop the others quickly.
+// Limits under 1 ms (the self-test limits) poll with test_wait, so that the
+// clock is read between polls however long try_wait would suspend.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag,
                                           uint64_t limit_ns = 4000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
+  const bool short_limit = limit_ns < 1000000ull;
+  if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))
+    return true;
+  const uint64_t t0 = globaltimer_ns();
   uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 255u) == 0) {
+    if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))
+      return true;
+    if (short_limit || (++spins & 255u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
@@ -298,6 +318,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 #undef LSR_W8
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ registers
+// Moves registers between the warpgroups of a block: every warp of a
+// warpgroup executes the same call.  An increase waits until decreases
+// elsewhere in the block have released enough registers, so the shares
+// must add up to at most the block's launch total (threads x registers
+// per thread at launch).
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------ math

@@ -51,6 +51,7 @@ SIGNATURES = {
                                  _P, _P, _P, _P, _P, _P, _Z, _P]),
     "lsr_pool_device_status": (_I, [_P, _PI, _P]),
     "lsr_selftest_bounded_wait": (_I, [_P, _I, _P]),
+    "lsr_pool_set_wait_limit": (_I, [_P, _I]),
     "lsr_group_rows": (_I, [_I, _I, _I, _P, _P]),
     "lsr_group_workspace_size": (_I, [_I, _I, _I, _I, _PZ]),
     "lsr_replay_group": (_I, [_P, _I, _P, _P, _P, _P, _P, _I, _I, _P, _I, _I,
@@ -453,6 +454,12 @@ def lsr_selftest_bounded_wait(dev_status: torch.Tensor, limit_us: int,
         raise TypeError("dev_status must be int32")
     _check(_lib.lsr_selftest_bounded_wait(_ptr(dev_status), limit_us,
                                           _stream(stream)))
+
+
+def lsr_pool_set_wait_limit(pool, limit_us: int):
+    """Limit (microseconds, 0 = default 4 s) of the attention kernels'
+    pipeline waits for later calls on `pool`."""
+    _check(_lib.lsr_pool_set_wait_limit(pool.handle, limit_us))
 
 
 def lsr_last_error() -> str:

@@ -50,3 +50,21 @@ def test_block_list_replays_in_reverse_and_covers_the_response():
     blocks = bench.block_list(1000, 3)
     assert [b[0] for b in blocks] == [666, 333, 0]
     assert sum(n for _, n in blocks) == 1000
+
+
+def test_tensor_rate_from_the_clock():
+    """The tensor core's rate is 8192 flop per clock per SM: at 152 SMs and
+    2070 MHz that is 2577.5 TFLOP/s, at 1900 MHz 2365.8."""
+    clocks = {"sm_mhz": 1900.0, "sm_max_mhz": 2070.0}
+    tp = bench.tensor_peaks(clocks)
+    scale = tp["sms"] / 152
+    assert math.isclose(tp["at_max_clock"], 2577.53088 * scale, rel_tol=1e-9)
+    assert math.isclose(tp["at_sampled_clock"], 2365.8496 * scale,
+                        rel_tol=1e-9)
+    peaks = {"bf16": 1890.7, "bf16_sustained": 1684.3, "source": "measured"}
+    r = bench.tensor_roofline("attn_bwd_dq", 1000.0, peaks, clocks, None)
+    assert math.isclose(r["frac"], 1000.0 / 1684.3)
+    assert math.isclose(r["frac_at_clock"], 1000.0 / tp["at_sampled_clock"])
+    pc = bench.peak_pcts(1000.0, peaks, clocks)
+    assert math.isclose(pc["pct_nominal_dense_bf16"], 100 * 1000 / 2250)
+    assert math.isclose(pc["pct_bf16_peak_burst"], 100 * 1000 / 1890.7)

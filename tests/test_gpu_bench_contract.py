@@ -40,6 +40,10 @@ def _check_line(d, steps, warmup):
         assert k in r, k
     assert r["bound"] == "tensor" and 0 < r["frac"] < 1.5
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    # the tensor core's own rate at the sampled clock bounds every kernel
+    assert 0 < r["frac_at_clock"] <= 1.0
+    assert abs(r["frac_at_clock"] * r["tensor_peak_at_clock"]
+               - r["achieved"]) < 1e-6 * r["achieved"]
     assert d["gpu_launches"] > 0
     c = d["clocks"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(c)
