@@ -126,9 +126,12 @@ lsr_status lsr_write_prefix_pages(lsr_pool_t pool, const void* k,
  *  P: prompt length (multiple of page_size).  The response keys
  *     0 .. resp_pos0 + R_b - 1 must already be in the pool.
  *  scale: softmax scale applied to q.k (e.g. 1/sqrt(head_dim)).
- *  m, l: device fp32 [num_shards+1][Hq][R_b]: row max of the scaled logits
- *     (natural-log units) and sum of exp(logit - m); an empty partial has
- *     m = -inf and l = 0.
+ *  m, l: device fp32 [num_shards+1][Hq][R_b]: a reference for the row's
+ *     scaled logits (natural-log units) and the sum of exp(logit - m)
+ *     against it; together they give the partial's log-sum-exp m + ln l.
+ *     m is ln 2 times an integer that lies at most 8 below and less than 1
+ *     above the row max in log2 units, so l stays within [2^-1, 2^8 n] for
+ *     n visible keys.  An empty partial has m = -inf and l = 0.
  *  o_part: device fp32 [num_shards+1][R_b][Hq][head_dim]: the partial
  *     output normalised by its own l (0 when empty).
  */

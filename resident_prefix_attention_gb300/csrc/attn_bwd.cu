@@ -51,7 +51,7 @@ struct __align__(1024) DqSmem {
   uint64_t k_empty[DqCfg<D, BN>::KST];
   uint64_t v_full[DqCfg<D, BN>::VST];
   uint64_t v_empty[DqCfg<D, BN>::VST];
-  uint64_t s_full[2], ds_full[2], dp_full, dp_free, dq_ready, mma_done;
+  uint64_t sdp_full, ds_full[2], dp_free, dq_ready, mma_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -90,11 +90,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.ds_full[i], 128);
-    }
-    mbar_init(&s.dp_full, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&s.ds_full[i], 128);
+    mbar_init(&s.sdp_full, 1);
     mbar_init(&s.dp_free, 128);
     mbar_init(&s.dq_ready, 1);
     mbar_init(&s.mma_done, 1);
@@ -158,46 +155,56 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Order: S_0, dP_0; then per step j: S_j+1, dP_j+1, dQ_j.  A commit holds
+    // the issuing warp until the products before it have entered the pipe,
+    // so each one is followed by a pipe bubble; there are two per step: one
+    // after S_j+1 and dP_j+1 (which the dS warps wait for) and one after
+    // dQ_j (which releases K_j's ring slot).  The dS warps release V's.
     if (n_tiles > 0) {  // the whole warp: one elected lane issues
       bool ok = warp_wait(&s.qd_full, 0, &s.abort_flag, p.wait_ns);
       // descriptors: one per operand tile, k-steps added as constants
       const uint64_t qd = sdesc(smem_u32(s.q), 16, 1024);
       const uint64_t dd = sdesc(smem_u32(s.dO), 16, 1024);
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles) {
-          const int ks = j % KST, vs = j % VST, b = j & 1;
-          if (!warp_wait(&s.k_full[ks], (j / KST) & 1, &s.abort_flag, p.wait_ns)) break;
-          tc_fence_after();
-          const uint64_t kd = sdesc(smem_u32(s.k[ks]), 16, 1024);
-          const uint64_t vd = sdesc(smem_u32(s.v[vs]), 16, 1024);
+      // S_i = Q K_i^T into S buffer i & 1, dP_i = dO V_i^T
+      auto issue_s_dp = [&](int i) -> bool {
+        const int ks = i % KST, vs = i % VST;
+        if (!warp_wait(&s.k_full[ks], (i / KST) & 1, &s.abort_flag, p.wait_ns))
+          return false;
+        tc_fence_after();
+        const uint64_t kd = sdesc(smem_u32(s.k[ks]), 16, 1024);
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_e(tm + b * BN, qd + kmaj_step<kTileRows>(k),
-                     kd + kmaj_step<BN>(k), C::ID_S, k > 0);
-          mma_commit_e(&s.s_full[b]);
-          if (j >= 1 && !warp_wait(&s.dp_free, (j - 1) & 1, &s.abort_flag, p.wait_ns))
-            break;
-          if (!warp_wait(&s.v_full[vs], (j / VST) & 1, &s.abort_flag, p.wait_ns)) break;
-          tc_fence_after();
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss_e(tm + (i & 1) * BN, qd + kmaj_step<kTileRows>(k),
+                   kd + kmaj_step<BN>(k), C::ID_S, k > 0);
+        // dP has one buffer: the dS warps have loaded dP_{i-1}
+        if (i >= 1 &&
+            !warp_wait(&s.dp_free, (i - 1) & 1, &s.abort_flag, p.wait_ns))
+          return false;
+        if (!warp_wait(&s.v_full[vs], (i / VST) & 1, &s.abort_flag, p.wait_ns))
+          return false;
+        tc_fence_after();
+        const uint64_t vd = sdesc(smem_u32(s.v[vs]), 16, 1024);
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss_e(tm + C::TM_DP, dd + kmaj_step<kTileRows>(k),
-                     vd + kmaj_step<BN>(k), C::ID_S, k > 0);
-          mma_commit_e(&s.dp_full);
-          mma_commit_e(&s.v_empty[vs]);
-        }
-        if (j >= 1) {
-          const int i = j - 1, ks = i % KST, b = i & 1;
-          if (!warp_wait(&s.ds_full[b], (i >> 1) & 1, &s.abort_flag, p.wait_ns)) break;
-          tc_fence_after();
-          // K as the MN-major B operand: 16 key rows of 128 bytes per step
-          const uint64_t kd = sdesc(smem_u32(s.k[ks]), BN * 128, 1024);
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss_e(tm + C::TM_DP, dd + kmaj_step<kTileRows>(k),
+                   vd + kmaj_step<BN>(k), C::ID_S, k > 0);
+        mma_commit_e(&s.sdp_full);
+        return true;
+      };
+      if (ok) ok = issue_s_dp(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles && !issue_s_dp(j + 1)) break;
+        const int ks = j % KST, b = j & 1;
+        if (!warp_wait(&s.ds_full[b], (j >> 1) & 1, &s.abort_flag, p.wait_ns))
+          break;
+        tc_fence_after();
+        // K as the MN-major B operand: 16 key rows of 128 bytes per step
+        const uint64_t kd = sdesc(smem_u32(s.k[ks]), BN * 128, 1024);
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k)
-            mma_ts_e(tm + C::TM_DQ, tm + b * BN + k * 8, kd + (uint64_t)k * 128,
-                     C::ID_DQ, (i > 0 || k > 0) ? 1u : 0u);
-          mma_commit_e(&s.k_empty[ks]);
-        }
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ts_e(tm + C::TM_DQ, tm + b * BN + k * 8, kd + (uint64_t)k * 128,
+                   C::ID_DQ, (j > 0 || k > 0) ? 1u : 0u);
+        mma_commit_e(&s.k_empty[ks]);
       }
       mma_commit_e(&s.dq_ready);
       mma_commit_e(&s.mma_done);
@@ -218,11 +225,14 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j & 1;
-      if (!warp_wait(&s.dp_full, j & 1, &s.abort_flag, p.wait_ns)) {
+      // S_j and dP_j are complete
+      if (!warp_wait(&s.sdp_full, j & 1, &s.abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // dP_j has read V_j: its ring slot is free
+      if (threadIdx.x == 64) mbar_arrive(&s.v_empty[j % VST]);
       // all of dP first, so the next dP product can start right away
       uint32_t dp[BN];
 #pragma unroll
@@ -230,11 +240,6 @@ __global__ void __launch_bounds__(192, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&s.dp_free);
-      if (!warp_wait(&s.s_full[b], (j >> 1) & 1, &s.abort_flag, p.wait_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       const int kbase = (rev ? n_tiles - 1 - j : j) * BN;
       const bool need_mask = kbase + BN - 1 > qpos;
 #pragma unroll
