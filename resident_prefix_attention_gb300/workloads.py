@@ -82,6 +82,12 @@ CONFIGS = {
                  shards=8, outlier_frac=0.001),
     "group": Config("group", P=1048576, R=4096, Hq=32, Hkv=8, d=128,
                     page_size=256, shards=8, G=8, r_min=512, r_max=4096),
+    # The 2M workload cut to one kv head (and its 4 query heads): the same
+    # key stream per kv head, the same CTAs per stream and per wave, with
+    # 1.07 GB of K/V instead of 8.6 GB.  Used for hardware-counter
+    # captures, whose DRAM traffic scales to 2M by the kv-head count.
+    "2M_kv1": Config("2M_kv1", P=2093056, R=4096, Hq=4, Hkv=1, d=128,
+                     page_size=256, shards=8, outlier_frac=0.001),
 }
 
 
