@@ -73,6 +73,8 @@ typedef enum {
 /* Bits of the device status word. */
 #define LSR_DEV_WAIT_TIMEOUT 1 /* a bounded in-kernel wait gave up */
 #define LSR_DEV_BAD_PAGE 2     /* a page-table entry was out of range */
+#define LSR_DEV_BOUNDS 4       /* debug build: an output index failed its
+                                  bounds check (the access was skipped) */
 
 typedef struct lsr_pool* lsr_pool_t;
 typedef struct lsr_window* lsr_window_t;

@@ -2,6 +2,11 @@
 
 Each CUDA translation unit is compiled in parallel with nvcc, then linked
 into one shared library next to this file.  Objects go to ``_build/``.
+
+With the environment variable ``LSR_DEBUG=1`` the kernels are built with
+their bounds checks (an output index outside its buffer sets
+``LSR_DEV_BOUNDS`` in the pool's status word and the access is skipped);
+the build records its flags and rebuilds when they change.
 """
 from __future__ import annotations
 
@@ -23,6 +28,12 @@ SOURCES = ["lsr_api.cu", "kernels_mem.cu", "attn_fwd.cu", "attn_bwd.cu",
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC",
          "-I" + os.path.join(ROOT, "include")] + ARCH
+STAMP = os.path.join(BUILD, "flags")
+
+
+def _flags():
+    debug = os.environ.get("LSR_DEBUG", "") not in ("", "0")
+    return FLAGS + (["-DLSR_DEBUG"] if debug else [])
 
 
 def _nvcc() -> str:
@@ -41,8 +52,11 @@ def _deps():
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
         return False
+    with open(STAMP) as f:
+        if f.read() != " ".join(_flags()):
+            return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
@@ -53,10 +67,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
+    flags = _flags()
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc, "-c", os.path.join(CSRC, src), "-o", obj] + FLAGS
+        cmd = [nvcc, "-c", os.path.join(CSRC, src), "-o", obj] + flags
         if verbose:
             cmd.append("-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -74,6 +89,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(" ".join(flags))
     return LIB
 
 

@@ -260,6 +260,9 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(&s.ds_full[b]);
     }
     float* drow = p.o + (((size_t)part * p.R_b + r) * p.Hq + h) * D;
+    // the dQ slice row lies inside the workspace's num_shards + 1 slices
+    const bool inb = valid && LSR_IN_BOUNDS(p, part <= p.num_shards &&
+                                                   r < p.R_b && h < p.Hq);
     if (ok && n_tiles > 0) {
       ok = warp_wait(&s.dq_ready, 0, &s.abort_flag, p.wait_ns);
       tc_fence_after();
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(192, 1)
           uint32_t o[32];
           tmem_ld32(lane_base + C::TM_DQ + c, o);
           tmem_ld_wait();
-          if (valid) {
+          if (inb) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               float4 f = make_float4(__uint_as_float(o[i]) * p.scale,
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-    } else if (n_tiles == 0 && valid) {
+    } else if (n_tiles == 0 && inb) {
       for (int c = 0; c < D; c += 4)
         *reinterpret_cast<float4*>(drow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -519,7 +522,11 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
     }
     if (ok && n_q > 0) {
-      const bool live = kj < nk_vis;
+      // the key's gradient page is one of the pages the call writes
+      const bool live =
+          kj < nk_vis &&
+          LSR_IN_BOUNDS(p, p.resp.gpage0[k_resp] + kj / p.ps < p.grad_pages &&
+                               g < p.Hkv);
       const size_t base =
           (((size_t)(p.resp.gpage0[k_resp] + kj / p.ps) * p.Hkv + g) * p.ps +
            kj % p.ps) * D;

@@ -26,8 +26,19 @@ struct AttnParams {
   float scale_log2;      // scale * log2(e)
   int num_sms;           // CTAs resident at once (one per SM)
   uint64_t wait_ns;      // limit of every pipeline wait (drains excepted)
+  int grad_pages;        // gradient pages the call writes (bounds checks)
   RespTable resp;        // which response each row of q belongs to
 };
+
+// Bounds checks of the debug build (compiled with -DLSR_DEBUG): a failed
+// check sets LSR_DEV_BOUNDS in the status word and the access is skipped.
+// In the release build every check is the constant true.
+#ifdef LSR_DEBUG
+#define LSR_IN_BOUNDS(p, cond) \
+  ((cond) ? true : (atomicOr((p).status, LSR_DEV_BOUNDS), false))
+#else
+#define LSR_IN_BOUNDS(p, cond) true
+#endif
 
 // Response owning row r of q (rows never straddle two responses in a CTA).
 __device__ __forceinline__ int resp_of_row(const AttnParams& p, int r) {
@@ -184,6 +195,14 @@ inline AttnParams make_params(const Pool& pl, const BlockGeom& g,
   p.scale_log2 = g.scale * kLog2e;
   p.num_sms = num_sms();
   p.wait_ns = pl.wait_ns;
+  // pages of the response gradient the call writes: every response's
+  // visible keys, from its first gradient page
+  p.grad_pages = 0;
+  for (int k = 0; k < g.resp.n; ++k) {
+    const int end =
+        g.resp.gpage0[k] + (g.resp.pos0[k] + g.resp.rows[k] + g.ps - 1) / g.ps;
+    if (end > p.grad_pages) p.grad_pages = end;
+  }
   return p;
 }
 

@@ -424,13 +424,16 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       if (ok) {
         const float inv = 1.f / lrnd;
+        const bool inb =
+            valid && LSR_IN_BOUNDS(p, part <= p.num_shards && r < p.R_b &&
+                                          h < p.Hq);
         float* orow = p.o + (((size_t)part * p.R_b + r) * p.Hq + h) * DV;
 #pragma unroll
         for (int c = 0; c < DV; c += 32) {
           uint32_t o[32];
           tmem_ld32(lane_base + o_col + c, o);
           tmem_ld_wait();
-          if (valid) {
+          if (inb) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               float4 f = make_float4(__uint_as_float(o[i]) * inv,
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
         }
-        if (valid) {
+        if (inb) {
           // (m, l): the reference in natural-log units and the sum of
           // exp(logit - m) against it
           const size_t si = ((size_t)part * p.Hq + h) * p.R_b + r;
@@ -449,7 +452,9 @@ __global__ void __launch_bounds__(384, 1)
           p.l[si] = lsum;
         }
       }
-    } else if (n_tiles == 0 && valid) {
+    } else if (n_tiles == 0 && valid &&
+               LSR_IN_BOUNDS(p, part <= p.num_shards && r < p.R_b &&
+                                    h < p.Hq)) {
       float* orow = p.o + (((size_t)part * p.R_b + r) * p.Hq + h) * DV;
       for (int c = 0; c < DV; c += 4)
         *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -29,6 +29,7 @@ LSR_ERR_DUPLICATE = 6
 LSR_ERR_STATE = 7
 LSR_DEV_WAIT_TIMEOUT = 1
 LSR_DEV_BAD_PAGE = 2
+LSR_DEV_BOUNDS = 4
 
 # Every function the header declares, with (restype, argtypes).
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
