@@ -346,29 +346,48 @@ __global__ void bwd_preprocess_kernel(const float* __restrict__ o,
   const int lane = threadIdx.x & 31;
   const size_t nrows = (size_t)R_b * Hq;
   const size_t wstride = (size_t)gridDim.x * (blockDim.x >> 5);
-  for (size_t row = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       row < nrows; row += wstride) {
-    const size_t base = row * (VEC * 32) + lane * VEC;
-    float acc = 0.f;
-    if constexpr (VEC == 4) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(o + base));
-      const uint2 b = __ldg(reinterpret_cast<const uint2*>(dO + base));
-      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
-      const float2 f0 = __bfloat1622float2(pb[0]);
-      const float2 f1 = __bfloat1622float2(pb[1]);
-      acc = a.x * f0.x + a.y * f0.y + a.z * f1.x + a.w * f1.y;
-    } else {
-      const float2 a = __ldg(reinterpret_cast<const float2*>(o + base));
-      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dO + base);
-      const float2 fb = __bfloat1622float2(b);
-      acc = a.x * fb.x + a.y * fb.y;
+  // RPW rows per warp at a time: their loads are all in flight before the
+  // first reduction
+  constexpr int RPW = 4;
+  for (size_t row0 =
+           ((size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW;
+       row0 < nrows; row0 += wstride * RPW) {
+    float acc[RPW];
+#pragma unroll
+    for (int k = 0; k < RPW; ++k) {
+      acc[k] = 0.f;
+      const size_t row = row0 + k;
+      if (row >= nrows) continue;
+      const size_t base = row * (VEC * 32) + lane * VEC;
+      if constexpr (VEC == 4) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(o + base));
+        const uint2 b = __ldg(reinterpret_cast<const uint2*>(dO + base));
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+        const float2 f0 = __bfloat1622float2(pb[0]);
+        const float2 f1 = __bfloat1622float2(pb[1]);
+        acc[k] = a.x * f0.x + a.y * f0.y + a.z * f1.x + a.w * f1.y;
+      } else {
+        const float2 a = __ldg(reinterpret_cast<const float2*>(o + base));
+        const __nv_bfloat162 b =
+            *reinterpret_cast<const __nv_bfloat162*>(dO + base);
+        const float2 fb = __bfloat1622float2(b);
+        acc[k] = a.x * fb.x + a.y * fb.y;
+      }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
+    for (int k = 0; k < RPW; ++k) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], off);
+    }
+    if (lane < RPW && row0 + lane < nrows) {
+      float a = acc[0];
+#pragma unroll
+      for (int k = 1; k < RPW; ++k)
+        if (lane == k) a = acc[k];
+      const size_t row = row0 + lane;
       const int r = (int)(row / Hq), h = (int)(row % Hq);
-      D[(size_t)h * R_b + r] = acc;
+      D[(size_t)h * R_b + r] = a;
     }
   }
 }
@@ -376,7 +395,7 @@ __global__ void bwd_preprocess_kernel(const float* __restrict__ o,
 cudaError_t launch_bwd_preprocess(const float* o, const void* dO, int Hq,
                                   int R_b, int d, float* D, cudaStream_t s) {
   const size_t rows = (size_t)R_b * Hq;
-  const int grid = grid_for(rows * 32, 256);
+  const int grid = grid_for((rows + 3) / 4 * 32, 256);  // four rows per warp
   if (d == 128)
     bwd_preprocess_kernel<4><<<grid, 256, 0, s>>>(
         o, (const __nv_bfloat16*)dO, Hq, R_b, D);
