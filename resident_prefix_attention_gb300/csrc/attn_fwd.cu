@@ -79,7 +79,7 @@ struct __align__(1024) FwdSmem {
   uint64_t q_full;
   uint64_t full[C::NS];
   uint64_t empty[C::NS];
-  uint64_t s_full[2], p_full[2], o_ready[2], o_final, mma_done;
+  uint64_t s_full[2], p_full[2], o_final, mma_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -192,7 +192,6 @@ __global__ void __launch_bounds__(384, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s.s_full[t], 1);
       mbar_init(&s.p_full[t], 128);
-      mbar_init(&s.o_ready[t], 1);
     }
     mbar_init(&s.o_final, 1);
     mbar_init(&s.mma_done, 1);
@@ -272,21 +271,28 @@ __global__ void __launch_bounds__(384, 1)
         issue_s<DQK, BN, C::ID_S>(tm, qd0, kd);
         mma_commit_e(&s.s_full[0]);
         issue_s<DQK, BN, C::ID_S>(tm + BN, qd1, kd);
+        // V_0 is waited for before the commit: a wait right behind a commit
+        // leaves the tensor pipe idle, one behind queued products costs
+        // nothing
+        if (!LAT && !warp_wait(&s.full[ring_v<LAT>(0) % NS], 0, &s.abort_flag,
+                               p.wait_ns))
+          ok = false;
         mma_commit_e(&s.s_full[1]);
-        if (!LAT) mma_commit_e(&s.empty[0]);
       }
+      // Two commits per key tile, one per query tile's S.  The softmax
+      // warps learn from them that the products issued earlier have run
+      // too: the previous PV of their tile (before an O rescale) and, for
+      // the second tile, every product that read K_j and V_{j-1} (they
+      // release those ring slots).
       for (int j = 0; ok && j < n_tiles; ++j) {
         const bool more = j + 1 < n_tiles;
         const int tv = ring_v<LAT>(j), sv = tv % NS;
         const int tk1 = ring_k<LAT>(j + 1), sk1 = tk1 % NS;
         // O0 += P0 V_j, then S0 of the next key tile over P0's columns
         if (!warp_wait(&s.p_full[0], j & 1, &s.abort_flag, p.wait_ns)) break;
-        if (!LAT && !warp_wait(&s.full[sv], (tv / NS) & 1, &s.abort_flag, p.wait_ns))
-          break;
         tc_fence_after();
         const uint64_t vd = sdesc(smem_u32(s.ring[sv]), BN * 128, 1024);
         issue_pv<BN, C::ID_PV>(tm + C::TM_O, tm + BN / 2, vd, j == 0);
-        mma_commit_e(&s.o_ready[0]);
         if (more) {
           if (!warp_wait(&s.full[sk1], (tk1 / NS) & 1, &s.abort_flag, p.wait_ns)) break;
           tc_fence_after();
@@ -299,14 +305,18 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         issue_pv<BN, C::ID_PV>(tm + C::TM_O + DV, tm + BN + BN / 2, vd,
                                j == 0);
-        mma_commit_e(&s.o_ready[1]);
-        // the tile's values have been read by both products
-        mma_commit_e(&s.empty[sv]);
+        // a latent key tile is also V_j: both PV products have read it
+        if (LAT) mma_commit_e(&s.empty[sv]);
         if (more) {
           issue_s<DQK, BN, C::ID_S>(tm + BN, qd1,
                                     sdesc(smem_u32(s.ring[sk1]), 16, 1024));
+          if (!LAT) {
+            const int tv1 = ring_v<LAT>(j + 1);
+            if (!warp_wait(&s.full[tv1 % NS], (tv1 / NS) & 1, &s.abort_flag,
+                           p.wait_ns))
+              break;
+          }
           mma_commit_e(&s.s_full[1]);
-          if (!LAT) mma_commit_e(&s.empty[sk1]);
         }
       }
       // A single-phase barrier for the epilogue (the per-tile barriers are
@@ -349,6 +359,12 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       tc_fence_after();
+      if (!LAT && t == 1 && threadIdx.x == 256) {
+        // S1_j has run, and with it every product issued before it: both
+        // S products of K_j and both PV products of V_{j-1}
+        mbar_arrive(&s.empty[ring_k<LAT>(j) % NS]);
+        if (j > 0) mbar_arrive(&s.empty[ring_v<LAT>(j - 1) % NS]);
+      }
       float x[BN];
 #pragma unroll
       for (int c = 0; c < BN; c += 32)
@@ -397,12 +413,7 @@ __global__ void __launch_bounds__(384, 1)
       lrnd += lr_t;
       if (j > 0 && rescale) {
         // S_t of this tile was issued after PV_t of the previous one, so
-        // that product is already complete; the wait documents it.
-        if (!warp_wait(&s.o_ready[t], (j - 1) & 1, &s.abort_flag, p.wait_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        // the s_full wait above has seen that product complete
 #pragma unroll
         for (int c = 0; c < DV; c += 32) {
           uint32_t o[32];
