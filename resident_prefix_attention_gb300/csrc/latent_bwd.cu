@@ -72,7 +72,7 @@ struct __align__(1024) LdqSmem {
 };
 
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     latent_bwd_dq_kernel(const __grid_constant__ CUtensorMap mq,
                          const __grid_constant__ CUtensorMap mdo,
                          const __grid_constant__ CUtensorMap mk,
@@ -99,9 +99,9 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&s.k_empty[i], 1);
     }
     mbar_init(&s.s_full, 1);
-    mbar_init(&s.s_free, 128);
+    mbar_init(&s.s_free, 256);
     mbar_init(&s.dp_full, 1);
-    mbar_init(&s.ds_full, 128);
+    mbar_init(&s.ds_full, 256);
     mbar_init(&s.dq_ready, 1);
     mbar_init(&s.mma_done, 1);
     s.abort_flag = 0;
@@ -206,7 +206,14 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------------------ dS warps
+    // Two warpgroups: a row's keys are split between warps w and w + 4
+    // (both own TMEM lanes 32*(w%4) .. +31), half of every key tile each.
+    // dS is elementwise in the keys, so the halves never exchange data,
+    // and the tile's dS is ready in half the time: it has to be before the
+    // product after S_{j+1}.
+    constexpr int HK = BN / 2;
     const int quarter = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int mrow = quarter * 32 + lane;
     const int r = r0 + mrow / p.G;
     const int h = mrow % p.G;
@@ -223,9 +230,10 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sv[BN];
+      uint32_t sv[HK];
 #pragma unroll
-      for (int c = 0; c < BN; c += 32) tmem_ld32(lane_base + C::TM_S + c, sv + c);
+      for (int c = 0; c < HK; c += 32)
+        tmem_ld32(lane_base + C::TM_S + hf * HK + c, sv + c);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&s.s_free);
@@ -234,12 +242,12 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      const int kbase = (rev ? n_tiles - 1 - j : j) * BN;
-      const bool need_mask = kbase + BN - 1 > qpos;
+      const int kbase = (rev ? n_tiles - 1 - j : j) * BN + hf * HK;
+      const bool need_mask = kbase + HK - 1 > qpos;
 #pragma unroll
-      for (int c = 0; c < BN; c += 32) {
+      for (int c = 0; c < HK; c += 32) {
         uint32_t dp[32], ds[16];
-        tmem_ld32(lane_base + C::TM_DP + c, dp);
+        tmem_ld32(lane_base + C::TM_DP + hf * HK + c, dp);
         tmem_ld_wait();
         if (need_mask)
           dq_chunk<true>(sv + c, dp, ds, p.scale_log2, lse2, Dv, kbase + c,
@@ -247,13 +255,15 @@ __global__ void __launch_bounds__(192, 1)
         else
           dq_chunk<false>(sv + c, dp, ds, p.scale_log2, lse2, Dv, kbase + c,
                           qpos);
-        tmem_st16(lane_base + C::TM_DS + c / 2, ds);
+        tmem_st16(lane_base + C::TM_DS + (hf * HK + c) / 2, ds);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.ds_full);
     }
-    float* drow = p.o + (((size_t)part * p.R_b + r) * p.Hq + h) * kDL;
+    // each half writes its kDL / 2 columns of the row
+    constexpr int HW = kDL / 2;
+    float* drow = p.o + (((size_t)part * p.R_b + r) * p.Hq + h) * kDL + hf * HW;
     // the dq~ slice row lies inside the workspace's num_shards + 1 slices
     const bool inb = valid && LSR_IN_BOUNDS(p, part <= p.num_shards &&
                                                    r < p.R_b && h < p.Hq);
@@ -262,9 +272,9 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       if (ok) {
 #pragma unroll
-        for (int c = 0; c < kDL; c += 32) {
+        for (int c = 0; c < HW; c += 32) {
           uint32_t o[32];
-          tmem_ld32(lane_base + C::TM_DQ + c, o);
+          tmem_ld32(lane_base + C::TM_DQ + hf * HW + c, o);
           tmem_ld_wait();
           if (inb) {
 #pragma unroll
@@ -279,7 +289,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     } else if (n_tiles == 0 && inb) {
-      for (int c = 0; c < kDL; c += 4)
+      for (int c = 0; c < HW; c += 4)
         *reinterpret_cast<float4*>(drow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
@@ -565,7 +575,7 @@ cudaError_t launch_latent_bwd_dq(const Pool& pl, const BlockGeom& g,
       reinterpret_cast<const void*>(latent_bwd_dq_kernel<128>), smem);
   if (e != cudaSuccess) return e;
   const int grid = g.n_qtiles * (g.num_shards + 1);
-  latent_bwd_dq_kernel<128><<<grid, 192, smem, s>>>(mq, mdo, mk, p);
+  latent_bwd_dq_kernel<128><<<grid, 320, smem, s>>>(mq, mdo, mk, p);
   return cudaGetLastError();
 }
 
