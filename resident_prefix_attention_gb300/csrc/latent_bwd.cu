@@ -66,7 +66,7 @@ struct __align__(1024) LdqSmem {
   uint64_t qd_full;
   uint64_t k_full[LdqCfg<BN>::KST];
   uint64_t k_empty[LdqCfg<BN>::KST];
-  uint64_t s_full, s_free, dp_full, ds_full, dq_ready, mma_done;
+  uint64_t sdp_full, sdp_free, ds_full, dq_ready, mma_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -98,9 +98,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.k_empty[i], 1);
     }
-    mbar_init(&s.s_full, 1);
-    mbar_init(&s.s_free, 256);
-    mbar_init(&s.dp_full, 1);
+    mbar_init(&s.sdp_full, 1);
+    mbar_init(&s.sdp_free, 256);
     mbar_init(&s.ds_full, 256);
     mbar_init(&s.dq_ready, 1);
     mbar_init(&s.mma_done, 1);
@@ -157,48 +156,48 @@ __global__ void __launch_bounds__(320, 1)
     if (n_tiles > 0) {  // the whole warp: one elected lane issues
       bool ok = warp_wait(&s.qd_full, 0, &s.abort_flag, p.wait_ns);
       const uint32_t qa = smem_u32(s.q), da = smem_u32(s.dO);
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        uint32_t ka = 0;
-        if (j < n_tiles) {
-          const int ks = j % KST;
-          if (!warp_wait(&s.k_full[ks], (j / KST) & 1, &s.abort_flag, p.wait_ns)) break;
-          // S columns free: the dS warps hold S_{j-1} in registers
-          if (j >= 1 && !warp_wait(&s.s_free, (j - 1) & 1, &s.abort_flag, p.wait_ns))
-            break;
-          tc_fence_after();
-          ka = smem_u32(s.k[ks]);
+      // Order: S_0, dP_0; then per step j: S_{j+1} and dP_{j+1} (one commit,
+      // which the dS warps wait for), dq~_j (one commit, which releases
+      // K_j's ring slot and tells the dS warps that dS_j has been read).
+      // The dS warps take S_j and dP_j into registers at once, so S_{j+1}
+      // and dP_{j+1} follow without waiting for dS_j, and dS_j has the
+      // time of dq~_{j-1}, S_{j+1} and dP_{j+1} to be ready.
+      auto issue_s_dp = [&](int i) -> bool {
+        const int ks = i % KST;
+        if (!warp_wait(&s.k_full[ks], (i / KST) & 1, &s.abort_flag, p.wait_ns))
+          return false;
+        // the dS warps hold S_{i-1} and dP_{i-1} in registers
+        if (i >= 1 &&
+            !warp_wait(&s.sdp_free, (i - 1) & 1, &s.abort_flag, p.wait_ns))
+          return false;
+        tc_fence_after();
+        const uint32_t ka = smem_u32(s.k[ks]);
 #pragma unroll
-          for (int k = 0; k < kDL / 16; ++k) {
-            mma_ss_e(tm + C::TM_S,
-                     sdesc(qa, 16, 1024) + kmaj_step<kTileRows>(k),
-                     sdesc(ka, 16, 1024) + kmaj_step<BN>(k), C::ID_S, k > 0);
-          }
-          mma_commit_e(&s.s_full);
-        }
-        if (j >= 1) {
-          // dq~ += dS_{j-1} L_{j-1}; dS_{j-1} complete also means dP_{j-1}
-          // has been read, so dP_j may follow
-          const int i = j - 1, ksi = i % KST;
-          if (!warp_wait(&s.ds_full, i & 1, &s.abort_flag, p.wait_ns)) break;
-          tc_fence_after();
-          const uint32_t kai = smem_u32(s.k[ksi]);
+        for (int k = 0; k < kDL / 16; ++k)
+          mma_ss_e(tm + C::TM_S, sdesc(qa, 16, 1024) + kmaj_step<kTileRows>(k),
+                   sdesc(ka, 16, 1024) + kmaj_step<BN>(k), C::ID_S, k > 0);
+        // dP = dO~ c^T: c is the first kDC columns of the key tile
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k)
-            mma_ts_e(tm + C::TM_DQ, tm + C::TM_DS + k * 8,
-                     sdesc(kai, BN * 128, 1024) + (uint64_t)k * 128, C::ID_DQ,
-                     (i > 0 || k > 0) ? 1u : 0u);
-          mma_commit_e(&s.k_empty[ksi]);
-        }
-        if (j < n_tiles) {
-          // dP_j = dO~ c_j^T: c is the first kDC columns of the key tile
+        for (int k = 0; k < kDC / 16; ++k)
+          mma_ss_e(tm + C::TM_DP, sdesc(da, 16, 1024) + kmaj_step<kTileRows>(k),
+                   sdesc(ka, 16, 1024) + kmaj_step<BN>(k), C::ID_S, k > 0);
+        mma_commit_e(&s.sdp_full);
+        return true;
+      };
+      if (ok) ok = issue_s_dp(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles && !issue_s_dp(j + 1)) break;
+        // dq~ += dS_j L_j
+        const int ks = j % KST;
+        if (!warp_wait(&s.ds_full, j & 1, &s.abort_flag, p.wait_ns)) break;
+        tc_fence_after();
+        const uint32_t ka = smem_u32(s.k[ks]);
 #pragma unroll
-          for (int k = 0; k < kDC / 16; ++k) {
-            mma_ss_e(tm + C::TM_DP,
-                     sdesc(da, 16, 1024) + kmaj_step<kTileRows>(k),
-                     sdesc(ka, 16, 1024) + kmaj_step<BN>(k), C::ID_S, k > 0);
-          }
-          mma_commit_e(&s.dp_full);
-        }
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ts_e(tm + C::TM_DQ, tm + C::TM_DS + k * 8,
+                   sdesc(ka, BN * 128, 1024) + (uint64_t)k * 128, C::ID_DQ,
+                   (j > 0 || k > 0) ? 1u : 0u);
+        mma_commit_e(&s.k_empty[ks]);
       }
       mma_commit_e(&s.dq_ready);
       mma_commit_e(&s.mma_done);
@@ -225,38 +224,43 @@ __global__ void __launch_bounds__(320, 1)
     const float Dv = valid ? p.Dvec[(size_t)h * p.R_b + r] : 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      if (!warp_wait(&s.s_full, j & 1, &s.abort_flag, p.wait_ns)) {
+      // S_j and dP_j are complete
+      if (!warp_wait(&s.sdp_full, j & 1, &s.abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sv[HK];
-#pragma unroll
-      for (int c = 0; c < HK; c += 32)
-        tmem_ld32(lane_base + C::TM_S + hf * HK + c, sv + c);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&s.s_free);
-      if (!warp_wait(&s.dp_full, j & 1, &s.abort_flag, p.wait_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int kbase = (rev ? n_tiles - 1 - j : j) * BN + hf * HK;
-      const bool need_mask = kbase + HK - 1 > qpos;
+      uint32_t sv[HK], dp[HK];
 #pragma unroll
       for (int c = 0; c < HK; c += 32) {
-        uint32_t dp[32], ds[16];
-        tmem_ld32(lane_base + C::TM_DP + hf * HK + c, dp);
-        tmem_ld_wait();
-        if (need_mask)
-          dq_chunk<true>(sv + c, dp, ds, p.scale_log2, lse2, Dv, kbase + c,
-                         qpos);
-        else
-          dq_chunk<false>(sv + c, dp, ds, p.scale_log2, lse2, Dv, kbase + c,
-                          qpos);
-        tmem_st16(lane_base + C::TM_DS + (hf * HK + c) / 2, ds);
+        tmem_ld32(lane_base + C::TM_S + hf * HK + c, sv + c);
+        tmem_ld32(lane_base + C::TM_DP + hf * HK + c, dp + c);
       }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&s.sdp_free);
+      const int kbase = (rev ? n_tiles - 1 - j : j) * BN + hf * HK;
+      const bool need_mask = kbase + HK - 1 > qpos;
+      uint32_t ds[HK / 2];
+#pragma unroll
+      for (int c = 0; c < HK; c += 32) {
+        if (need_mask)
+          dq_chunk<true>(sv + c, dp + c, ds + c / 2, p.scale_log2, lse2, Dv,
+                         kbase + c, qpos);
+        else
+          dq_chunk<false>(sv + c, dp + c, ds + c / 2, p.scale_log2, lse2, Dv,
+                          kbase + c, qpos);
+      }
+      // dq~_{j-1} has read dS_{j-1}: its commit also released K_{j-1}
+      if (j >= 1 && !warp_wait(&s.k_empty[(j - 1) % KST], ((j - 1) / KST) & 1,
+                               &s.abort_flag, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < HK / 2; c += 16)
+        tmem_st16(lane_base + C::TM_DS + hf * (HK / 2) + c, ds + c);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&s.ds_full);
