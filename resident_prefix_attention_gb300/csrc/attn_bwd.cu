@@ -47,9 +47,8 @@ struct __align__(1024) DqSmem {
   __nv_bfloat16 k[DqCfg<D, BN>::KST][BN * D];
   __nv_bfloat16 v[DqCfg<D, BN>::VST][BN * D];
   uint64_t qd_full;
-  uint64_t k_full[DqCfg<D, BN>::KST];
+  uint64_t k_full[DqCfg<D, BN>::KST];  // K_j and V_j (one barrier per step)
   uint64_t k_empty[DqCfg<D, BN>::KST];
-  uint64_t v_full[DqCfg<D, BN>::VST];
   uint64_t v_empty[DqCfg<D, BN>::VST];
   uint64_t sdp_full, ds_full[2], dp_free, dq_ready, mma_done;
   uint32_t tmem_base;
@@ -86,10 +85,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.k_empty[i], 1);
     }
-    for (int i = 0; i < VST; ++i) {
-      mbar_init(&s.v_full[i], 1);
-      mbar_init(&s.v_empty[i], 1);
-    }
+    for (int i = 0; i < VST; ++i) mbar_init(&s.v_empty[i], 1);
     for (int i = 0; i < 2; ++i) mbar_init(&s.ds_full[i], 128);
     mbar_init(&s.sdp_full, 1);
     mbar_init(&s.dp_free, 128);
@@ -125,41 +121,39 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_3d_e(s.dO + c * kTileRows * 64, &mdo, &s.qd_full, c * 64,
                       g * p.G, r0);
       }
-      int k_issued = 0, v_issued = 0;
+      int k_issued = 0;
       for (int j = 0; j < n_tiles; ++j) {
         const int row = pool_row(p, kr.page0, (rev ? n_tiles - 1 - j : j) * BN, g);
         const int ks = j % KST, vs = j % VST;
         if (j >= KST &&
             !warp_wait(&s.k_empty[ks], ((j / KST) & 1) ^ 1, &s.abort_flag, p.wait_ns))
           break;
-        mbar_expect_tx_e(&s.k_full[ks], C::KV_BYTES);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_2d_e(s.k[ks] + c * BN * 64, &mk, &s.k_full[ks], c * 64, row);
-        k_issued = j + 1;
         if (j >= VST &&
             !warp_wait(&s.v_empty[vs], ((j / VST) & 1) ^ 1, &s.abort_flag, p.wait_ns))
           break;
-        mbar_expect_tx_e(&s.v_full[vs], C::KV_BYTES);
+        // K_j and V_j land on one barrier
+        mbar_expect_tx_e(&s.k_full[ks], 2 * C::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_2d_e(s.v[vs] + c * BN * 64, &mv, &s.v_full[vs], c * 64, row);
-        v_issued = j + 1;
+          tma_load_2d_e(s.k[ks] + c * BN * 64, &mk, &s.k_full[ks], c * 64, row);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d_e(s.v[vs] + c * BN * 64, &mv, &s.k_full[ks], c * 64, row);
+        k_issued = j + 1;
       }
       // every copy lands before the CTA can exit (see the forward kernel)
       mbar_wait_drain(&s.qd_full, 0);
       for (int t = max(0, k_issued - KST); t < k_issued; ++t)
         mbar_wait_drain(&s.k_full[t % KST], (t / KST) & 1);
-      for (int t = max(0, v_issued - VST); t < v_issued; ++t)
-        mbar_wait_drain(&s.v_full[t % VST], (t / VST) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Order: S_0, dP_0; then per step j: S_j+1, dP_j+1, dQ_j.  A commit holds
-    // the issuing warp until the products before it have entered the pipe,
-    // so each one is followed by a pipe bubble; there are two per step: one
-    // after S_j+1 and dP_j+1 (which the dS warps wait for) and one after
-    // dQ_j (which releases K_j's ring slot).  The dS warps release V's.
+    // Order: S_0, dP_0; then per step j: S_j+1, dP_j+1, dQ_j.  Every commit
+    // and every wait of this warp costs the tensor pipe time, so there are
+    // two commits per step (one after S_j+1 and dP_j+1, which the dS warps
+    // wait for; one after dQ_j, which releases K_j's ring slot) and three
+    // waits (K_j+1 and V_j+1 on one barrier, dP's buffer, dS_j).  The dS
+    // warps release V's slots.
     if (n_tiles > 0) {  // the whole warp: one elected lane issues
       bool ok = warp_wait(&s.qd_full, 0, &s.abort_flag, p.wait_ns);
       // descriptors: one per operand tile, k-steps added as constants
@@ -179,8 +173,6 @@ __global__ void __launch_bounds__(192, 1)
         // dP has one buffer: the dS warps have loaded dP_{i-1}
         if (i >= 1 &&
             !warp_wait(&s.dp_free, (i - 1) & 1, &s.abort_flag, p.wait_ns))
-          return false;
-        if (!warp_wait(&s.v_full[vs], (i / VST) & 1, &s.abort_flag, p.wait_ns))
           return false;
         tc_fence_after();
         const uint64_t vd = sdesc(smem_u32(s.v[vs]), 16, 1024);

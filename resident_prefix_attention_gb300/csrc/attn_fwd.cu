@@ -79,6 +79,7 @@ struct __align__(1024) FwdSmem {
   uint64_t q_full;
   uint64_t full[C::NS];
   uint64_t empty[C::NS];
+  uint64_t step_full[3];  // K/V pages: K_j and V_j land on step_full[j % 3]
   uint64_t s_full[2], p_full[2], o_final, mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&s.s_full[t], 1);
       mbar_init(&s.p_full[t], 128);
     }
+    for (int i = 0; i < 3; ++i) mbar_init(&s.step_full[i], 1);
     mbar_init(&s.o_final, 1);
     mbar_init(&s.mma_done, 1);
     s.abort_flag = 0;
@@ -224,38 +226,49 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < DQK / 64; ++c)
           tma_load_3d_e(s.q[t] + c * kTileRows * 64, &mq, &s.q_full, c * 64,
                         g * p.G, r0 + t * p.rows_per_tile);
-      int issued = 0;  // ring tiles issued
+      int issued = 0;  // ring tiles issued (latent) or key tiles (K/V)
       for (int j = 0; j < n_tiles; ++j) {
         const int row = pool_row(p, kr.page0, (rev ? n_tiles - 1 - j : j) * BN, g);
         const int tk = ring_k<LAT>(j), sk = tk % NS;
         if (tk >= NS &&
             !warp_wait(&s.empty[sk], ((tk / NS) & 1) ^ 1, &s.abort_flag, p.wait_ns))
           break;
-        mbar_expect_tx_e(&s.full[sk], C::K_BYTES);
+        if (LAT) {
+          mbar_expect_tx_e(&s.full[sk], C::K_BYTES);
 #pragma unroll
-        for (int c = 0; c < DQK / 64; ++c)
-          tma_load_2d_e(s.ring[sk] + c * BN * 64, &mk, &s.full[sk], c * 64,
-                        row);
-        issued = tk + 1;
-        if (LAT) continue;
+          for (int c = 0; c < DQK / 64; ++c)
+            tma_load_2d_e(s.ring[sk] + c * BN * 64, &mk, &s.full[sk], c * 64,
+                          row);
+          issued = tk + 1;
+          continue;
+        }
         const int tv = ring_v<LAT>(j), sv = tv % NS;
         if (tv >= NS &&
             !warp_wait(&s.empty[sv], ((tv / NS) & 1) ^ 1, &s.abort_flag, p.wait_ns))
           break;
-        mbar_expect_tx_e(&s.full[sv], C::V_BYTES);
+        // K_j and V_j land on one barrier: one wait for the MMA warp
+        uint64_t* bar = &s.step_full[j % 3];
+        mbar_expect_tx_e(bar, C::K_BYTES + C::V_BYTES);
+#pragma unroll
+        for (int c = 0; c < DQK / 64; ++c)
+          tma_load_2d_e(s.ring[sk] + c * BN * 64, &mk, bar, c * 64, row);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_2d_e(s.ring[sv] + c * BN * 64, &mv, &s.full[sv], c * 64,
-                        row);
-        issued = tv + 1;
+          tma_load_2d_e(s.ring[sv] + c * BN * 64, &mv, bar, c * 64, row);
+        issued = j + 1;
       }
       // Every copy lands before the CTA can exit.  After a normal run the
       // consumers have already waited for all of them; after an abort
       // (any role's wait ran out) this keeps late copies out of the shared
       // memory of whatever CTA runs next on the SM.
       mbar_wait_drain(&s.q_full, 0);
-      for (int t = max(0, issued - NS); t < issued; ++t)
-        mbar_wait_drain(&s.full[t % NS], (t / NS) & 1);
+      if (LAT) {
+        for (int t = max(0, issued - NS); t < issued; ++t)
+          mbar_wait_drain(&s.full[t % NS], (t / NS) & 1);
+      } else {
+        for (int t = max(0, issued - 3); t < issued; ++t)
+          mbar_wait_drain(&s.step_full[t % 3], (t / 3) & 1);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -263,20 +276,22 @@ __global__ void __launch_bounds__(384, 1)
     if (n_tiles > 0) {  // the whole warp: one elected lane issues
       const uint64_t qd0 = sdesc(smem_u32(s.q[0]), 16, 1024);
       const uint64_t qd1 = sdesc(smem_u32(s.q[1]), 16, 1024);
+      // key tile j (and V_j) has landed
+      auto tile_wait = [&](int j) -> bool {
+        return LAT ? warp_wait(&s.full[ring_k<LAT>(j) % NS],
+                               (ring_k<LAT>(j) / NS) & 1, &s.abort_flag,
+                               p.wait_ns)
+                   : warp_wait(&s.step_full[j % 3], (j / 3) & 1, &s.abort_flag,
+                               p.wait_ns);
+      };
       bool ok = warp_wait(&s.q_full, 0, &s.abort_flag, p.wait_ns) &&
-                warp_wait(&s.full[0], 0, &s.abort_flag, p.wait_ns);
+                tile_wait(0);
       if (ok) {
         tc_fence_after();
         const uint64_t kd = sdesc(smem_u32(s.ring[0]), 16, 1024);
         issue_s<DQK, BN, C::ID_S>(tm, qd0, kd);
         mma_commit_e(&s.s_full[0]);
         issue_s<DQK, BN, C::ID_S>(tm + BN, qd1, kd);
-        // V_0 is waited for before the commit: a wait right behind a commit
-        // leaves the tensor pipe idle, one behind queued products costs
-        // nothing
-        if (!LAT && !warp_wait(&s.full[ring_v<LAT>(0) % NS], 0, &s.abort_flag,
-                               p.wait_ns))
-          ok = false;
         mma_commit_e(&s.s_full[1]);
       }
       // Two commits per key tile, one per query tile's S.  The softmax
@@ -294,7 +309,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint64_t vd = sdesc(smem_u32(s.ring[sv]), BN * 128, 1024);
         issue_pv<BN, C::ID_PV>(tm + C::TM_O, tm + BN / 2, vd, j == 0);
         if (more) {
-          if (!warp_wait(&s.full[sk1], (tk1 / NS) & 1, &s.abort_flag, p.wait_ns)) break;
+          if (!tile_wait(j + 1)) break;
           tc_fence_after();
           issue_s<DQK, BN, C::ID_S>(tm, qd0,
                                     sdesc(smem_u32(s.ring[sk1]), 16, 1024));
@@ -310,12 +325,6 @@ __global__ void __launch_bounds__(384, 1)
         if (more) {
           issue_s<DQK, BN, C::ID_S>(tm + BN, qd1,
                                     sdesc(smem_u32(s.ring[sk1]), 16, 1024));
-          if (!LAT) {
-            const int tv1 = ring_v<LAT>(j + 1);
-            if (!warp_wait(&s.full[tv1 % NS], (tv1 / NS) & 1, &s.abort_flag,
-                           p.wait_ns))
-              break;
-          }
           mma_commit_e(&s.s_full[1]);
         }
       }
