@@ -79,7 +79,9 @@ struct __align__(1024) FwdSmem {
   uint64_t q_full;
   uint64_t full[C::NS];
   uint64_t empty[C::NS];
-  uint64_t step_full[3];  // K/V pages: K_j and V_j land on step_full[j % 3]
+  // K/V pages: group 0 is K_0, group g > 0 is V_{g-1} and K_g (the ring
+  // tiles between two S products); group g lands on step_full[g % 3]
+  uint64_t step_full[3];
   uint64_t s_full[2], p_full[2], o_final, mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -242,20 +244,41 @@ __global__ void __launch_bounds__(384, 1)
           issued = tk + 1;
           continue;
         }
-        const int tv = ring_v<LAT>(j), sv = tv % NS;
-        if (tv >= NS &&
-            !warp_wait(&s.empty[sv], ((tv / NS) & 1) ^ 1, &s.abort_flag, p.wait_ns))
-          break;
-        // K_j and V_j land on one barrier: one wait for the MMA warp
+        // group j: V_{j-1} (issued with it) and K_j
         uint64_t* bar = &s.step_full[j % 3];
-        mbar_expect_tx_e(bar, C::K_BYTES + C::V_BYTES);
+        if (j > 0) {
+          const int tv = ring_v<LAT>(j - 1), sv = tv % NS;
+          if (tv >= NS &&
+              !warp_wait(&s.empty[sv], ((tv / NS) & 1) ^ 1, &s.abort_flag, p.wait_ns))
+            break;
+        }
+        mbar_expect_tx_e(bar, C::K_BYTES + (j > 0 ? C::V_BYTES : 0));
+        if (j > 0) {
+          const int sv = ring_v<LAT>(j - 1) % NS;
+          const int rowv = pool_row(p, kr.page0, (rev ? n_tiles - j : j - 1) * BN, g);
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_2d_e(s.ring[sv] + c * BN * 64, &mv, bar, c * 64, rowv);
+        }
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
           tma_load_2d_e(s.ring[sk] + c * BN * 64, &mk, bar, c * 64, row);
-#pragma unroll
-        for (int c = 0; c < DV / 64; ++c)
-          tma_load_2d_e(s.ring[sv] + c * BN * 64, &mv, bar, c * 64, row);
         issued = j + 1;
+      }
+      // the last group: V_{n-1} alone
+      if (!LAT && issued == n_tiles && n_tiles > 0) {
+        const int j = n_tiles;
+        const int tv = ring_v<LAT>(j - 1), sv = tv % NS;
+        if (tv < NS ||
+            warp_wait(&s.empty[sv], ((tv / NS) & 1) ^ 1, &s.abort_flag, p.wait_ns)) {
+          uint64_t* bar = &s.step_full[j % 3];
+          mbar_expect_tx_e(bar, C::V_BYTES);
+          const int rowv = pool_row(p, kr.page0, (rev ? 0 : j - 1) * BN, g);
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_2d_e(s.ring[sv] + c * BN * 64, &mv, bar, c * 64, rowv);
+          issued = j + 1;
+        }
       }
       // Every copy lands before the CTA can exit.  After a normal run the
       // consumers have already waited for all of them; after an abort
@@ -276,7 +299,7 @@ __global__ void __launch_bounds__(384, 1)
     if (n_tiles > 0) {  // the whole warp: one elected lane issues
       const uint64_t qd0 = sdesc(smem_u32(s.q[0]), 16, 1024);
       const uint64_t qd1 = sdesc(smem_u32(s.q[1]), 16, 1024);
-      // key tile j (and V_j) has landed
+      // latent: key tile j has landed; K/V pages: group j (V_{j-1}, K_j)
       auto tile_wait = [&](int j) -> bool {
         return LAT ? warp_wait(&s.full[ring_k<LAT>(j) % NS],
                                (ring_k<LAT>(j) / NS) & 1, &s.abort_flag,
@@ -303,14 +326,20 @@ __global__ void __launch_bounds__(384, 1)
         const bool more = j + 1 < n_tiles;
         const int tv = ring_v<LAT>(j), sv = tv % NS;
         const int tk1 = ring_k<LAT>(j + 1), sk1 = tk1 % NS;
+        // V_j and K_{j+1} have landed (waited for before P0, so that PV0 and
+        // S0 go out back to back: a wait between the products of a group
+        // leaves the tensor pipe idle)
+        if (!LAT && !tile_wait(j + 1)) break;
         // O0 += P0 V_j, then S0 of the next key tile over P0's columns
         if (!warp_wait(&s.p_full[0], j & 1, &s.abort_flag, p.wait_ns)) break;
         tc_fence_after();
         const uint64_t vd = sdesc(smem_u32(s.ring[sv]), BN * 128, 1024);
         issue_pv<BN, C::ID_PV>(tm + C::TM_O, tm + BN / 2, vd, j == 0);
         if (more) {
-          if (!tile_wait(j + 1)) break;
-          tc_fence_after();
+          if (LAT) {
+            if (!tile_wait(j + 1)) break;
+            tc_fence_after();
+          }
           issue_s<DQK, BN, C::ID_S>(tm, qd0,
                                     sdesc(smem_u32(s.ring[sk1]), 16, 1024));
           mma_commit_e(&s.s_full[0]);
