@@ -9,16 +9,16 @@
 // rows (128/Hq positions x Hq heads) against one partial.  Per key tile:
 // S = q~ L^T, dP = dO~ c^T, P = exp(S*scale - lse), dS = P * (dP - D), and
 // dq~ += dS L.  A 192-column dq~ accumulator leaves no room in the 512 TMEM
-// columns for a second S buffer, so the schedule differs from the K/V dQ
-// pass:
+// columns for a second S buffer:
 //   TMEM: S [0,128), dP [128,256), dq~ [256,448), dS (bf16 pairs) [448,512)
-//   - the dS warpgroup first loads all of S_j into registers, which frees
-//     the S columns at once, then walks dP_j in 32-column chunks and writes
-//     dS_j to its own columns;
-//   - the MMA order S_j, dq~ += dS_{j-1} L_{j-1}, dP_j keeps the tensor pipe
-//     on S_{j+1} while dS_j is being computed, and the completion of dP_j
-//     implies that of the dq~ product reading dS_{j-1}, so dS_j may
-//     overwrite it.
+//   - two dS warpgroups, each taking half of a tile's keys, first load all
+//     of their S_j and dP_j into registers, which frees both buffers at
+//     once;
+//   - the MMA order is the K/V dQ pass's: S_{j+1} and dP_{j+1} under one
+//     commit, then dq~ += dS_j L_j under another, so dS_j has the time of
+//     dq~_{j-1}, S_{j+1} and dP_{j+1} to be ready;
+//   - the dS warps write dS_j once the commit after dq~_{j-1} shows that
+//     product has read dS_{j-1}.
 // The key tile in shared memory serves S, dP (its first two 64-column
 // boxes are c) and dq~; it is freed after the dq~ product.
 //
@@ -207,9 +207,8 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ dS warps
     // Two warpgroups: a row's keys are split between warps w and w + 4
     // (both own TMEM lanes 32*(w%4) .. +31), half of every key tile each.
-    // dS is elementwise in the keys, so the halves never exchange data,
-    // and the tile's dS is ready in half the time: it has to be before the
-    // product after S_{j+1}.
+    // dS is elementwise in the keys, so the halves never exchange data.
+    // Each thread holds its half of S_j and dP_j (64 + 64 registers).
     constexpr int HK = BN / 2;
     const int quarter = warp & 3;
     const int hf = (warp - 2) >> 2;
