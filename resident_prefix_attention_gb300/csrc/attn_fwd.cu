@@ -23,9 +23,10 @@
 // Latent pages (LAT = true): one latent row [c, r] per position is both the
 // key (all DQK columns) and, through its first DV columns, the value, for
 // every query head (MLA-style resident state, the GLM bullet of the same
-// section).  The ring's key tiles then also feed the PV products, so a
-// key tile stays resident until both PV products have read it, and no V
-// tile is loaded.
+// section).  No V tile is loaded: the key tile's c part feeds the PV
+// products.  It sits in the ring until both PV products have read it,
+// while the r part sits in a ring of its own that frees as soon as both S
+// products have run.
 #include <cmath>
 #include <climits>
 #include "attn_common.cuh"
@@ -40,8 +41,15 @@ struct FwdCfg {
   // One ring of key-tile slots.  K/V pages: K_j and V_j are ring tiles 2j
   // and 2j+1 (DQK == DV, so both fit a slot), loaded and released in that
   // order, so both kinds of tile get the same lead over their use.  Latent
-  // pages: ring tile j is key tile j, whose first DV columns are V_j.
-  static constexpr int NS = LAT ? 2 : (kStd128 ? 5 : 8);
+  // pages: ring tile j holds the first DV columns of key tile j (c, which
+  // is also V_j); its last DQK - DV columns (r) go to a second ring of NSR
+  // slots.  The r part is free once both S products have run, the c part
+  // only after both PV products, so the split gives the c part a third
+  // slot of lead in the same shared memory.
+  static constexpr int NS = LAT ? 3 : (kStd128 ? 5 : 8);
+  static constexpr int NSR = 2;
+  static constexpr int RING_COLS = LAT ? DV : DQK;  // columns of a ring slot
+  static constexpr int R_COLS = LAT ? DQK - DV : 64;  // of an r slot
   static constexpr int Q_BYTES = kTileRows * DQK * 2;
   static constexpr int K_BYTES = BN * DQK * 2;
   static constexpr int V_BYTES = BN * DV * 2;
@@ -75,26 +83,33 @@ template <int DQK, int DV, int BN, bool LAT>
 struct __align__(1024) FwdSmem {
   using C = FwdCfg<DQK, DV, BN, LAT>;
   __nv_bfloat16 q[2][kTileRows * DQK];
-  __nv_bfloat16 ring[C::NS][BN * DQK];
+  __nv_bfloat16 ring[C::NS][BN * C::RING_COLS];
+  __nv_bfloat16 rring[LAT ? C::NSR : 1][LAT ? BN * C::R_COLS : 64];
   uint64_t q_full;
   uint64_t full[C::NS];
   uint64_t empty[C::NS];
+  uint64_t r_empty[C::NSR];  // latent pages: the r slots
   // K/V pages: group 0 is K_0, group g > 0 is V_{g-1} and K_g (the ring
-  // tiles between two S products); group g lands on step_full[g % 3]
+  // tiles between two S products); group g lands on step_full[g % 3].
+  // Latent pages: both parts of key tile g land on step_full[g % 3].
   uint64_t step_full[3];
   uint64_t s_full[2], p_full[2], o_final, mma_done;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// S = Q K^T over DQK/16 k-steps; qd, kd: descriptors of the two tiles
-template <int DQK, int BN, uint32_t ID>
+// S = Q K^T over DQK/16 k-steps; qd, kd: descriptors of the two tiles.
+// The key tile's first KC columns are at kd, the rest (latent pages: the r
+// part, in its own ring) at kd2.
+template <int DQK, int KC, int BN, uint32_t ID>
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t qd,
-                                        uint64_t kd) {
+                                        uint64_t kd, uint64_t kd2) {
 #pragma unroll
   for (int k = 0; k < DQK / 16; ++k)
-    mma_ss_e(d_tmem, qd + kmaj_step<kTileRows>(k), kd + kmaj_step<BN>(k), ID,
-             k > 0);
+    mma_ss_e(d_tmem, qd + kmaj_step<kTileRows>(k),
+             k < KC / 16 ? kd + kmaj_step<BN>(k)
+                         : kd2 + kmaj_step<BN>(k - KC / 16),
+             ID, k > 0);
 }
 
 // O += P V with V the first DV columns of a [BN][.] tile stored as 64-column
@@ -197,6 +212,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&s.p_full[t], 128);
     }
     for (int i = 0; i < 3; ++i) mbar_init(&s.step_full[i], 1);
+    for (int i = 0; i < C::NSR; ++i) mbar_init(&s.r_empty[i], 1);
     mbar_init(&s.o_final, 1);
     mbar_init(&s.mma_done, 1);
     s.abort_flag = 0;
@@ -236,12 +252,22 @@ __global__ void __launch_bounds__(384, 1)
             !warp_wait(&s.empty[sk], ((tk / NS) & 1) ^ 1, &s.abort_flag, p.wait_ns))
           break;
         if (LAT) {
-          mbar_expect_tx_e(&s.full[sk], C::K_BYTES);
+          // c part into ring slot sk, r part into r slot j % NSR
+          const int sr = j % C::NSR;
+          if (j >= C::NSR &&
+              !warp_wait(&s.r_empty[sr], ((j / C::NSR) & 1) ^ 1, &s.abort_flag,
+                         p.wait_ns))
+            break;
+          uint64_t* bar = &s.step_full[j % 3];
+          mbar_expect_tx_e(bar, C::K_BYTES);
 #pragma unroll
-          for (int c = 0; c < DQK / 64; ++c)
-            tma_load_2d_e(s.ring[sk] + c * BN * 64, &mk, &s.full[sk], c * 64,
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_2d_e(s.ring[sk] + c * BN * 64, &mk, bar, c * 64, row);
+#pragma unroll
+          for (int c = 0; c < C::R_COLS / 64; ++c)
+            tma_load_2d_e(s.rring[sr] + c * BN * 64, &mk, bar, DV + c * 64,
                           row);
-          issued = tk + 1;
+          issued = j + 1;
           continue;
         }
         // group j: V_{j-1} (issued with it) and K_j
@@ -285,13 +311,8 @@ __global__ void __launch_bounds__(384, 1)
       // (any role's wait ran out) this keeps late copies out of the shared
       // memory of whatever CTA runs next on the SM.
       mbar_wait_drain(&s.q_full, 0);
-      if (LAT) {
-        for (int t = max(0, issued - NS); t < issued; ++t)
-          mbar_wait_drain(&s.full[t % NS], (t / NS) & 1);
-      } else {
-        for (int t = max(0, issued - 3); t < issued; ++t)
-          mbar_wait_drain(&s.step_full[t % 3], (t / 3) & 1);
-      }
+      for (int t = max(0, issued - 3); t < issued; ++t)
+        mbar_wait_drain(&s.step_full[t % 3], (t / 3) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -301,20 +322,25 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t qd1 = sdesc(smem_u32(s.q[1]), 16, 1024);
       // latent: key tile j has landed; K/V pages: group j (V_{j-1}, K_j)
       auto tile_wait = [&](int j) -> bool {
-        return LAT ? warp_wait(&s.full[ring_k<LAT>(j) % NS],
-                               (ring_k<LAT>(j) / NS) & 1, &s.abort_flag,
-                               p.wait_ns)
-                   : warp_wait(&s.step_full[j % 3], (j / 3) & 1, &s.abort_flag,
-                               p.wait_ns);
+        return warp_wait(&s.step_full[j % 3], (j / 3) & 1, &s.abort_flag,
+                         p.wait_ns);
       };
+      // descriptors of key tile j's parts (the r slot only for latent pages)
+      auto kdesc = [&](int j) {
+        return sdesc(smem_u32(s.ring[ring_k<LAT>(j) % NS]), 16, 1024);
+      };
+      auto rdesc = [&](int j) {
+        return sdesc(smem_u32(s.rring[LAT ? j % C::NSR : 0]), 16, 1024);
+      };
+      constexpr int KC = C::RING_COLS;
       bool ok = warp_wait(&s.q_full, 0, &s.abort_flag, p.wait_ns) &&
                 tile_wait(0);
       if (ok) {
         tc_fence_after();
-        const uint64_t kd = sdesc(smem_u32(s.ring[0]), 16, 1024);
-        issue_s<DQK, BN, C::ID_S>(tm, qd0, kd);
+        const uint64_t kd = kdesc(0), kd2 = rdesc(0);
+        issue_s<DQK, KC, BN, C::ID_S>(tm, qd0, kd, kd2);
         mma_commit_e(&s.s_full[0]);
-        issue_s<DQK, BN, C::ID_S>(tm + BN, qd1, kd);
+        issue_s<DQK, KC, BN, C::ID_S>(tm + BN, qd1, kd, kd2);
         mma_commit_e(&s.s_full[1]);
       }
       // Two commits per key tile, one per query tile's S.  The softmax
@@ -325,7 +351,6 @@ __global__ void __launch_bounds__(384, 1)
       for (int j = 0; ok && j < n_tiles; ++j) {
         const bool more = j + 1 < n_tiles;
         const int tv = ring_v<LAT>(j), sv = tv % NS;
-        const int tk1 = ring_k<LAT>(j + 1), sk1 = tk1 % NS;
         // V_j and K_{j+1} have landed (waited for before P0, so that PV0 and
         // S0 go out back to back: a wait between the products of a group
         // leaves the tensor pipe idle)
@@ -340,8 +365,7 @@ __global__ void __launch_bounds__(384, 1)
             if (!tile_wait(j + 1)) break;
             tc_fence_after();
           }
-          issue_s<DQK, BN, C::ID_S>(tm, qd0,
-                                    sdesc(smem_u32(s.ring[sk1]), 16, 1024));
+          issue_s<DQK, KC, BN, C::ID_S>(tm, qd0, kdesc(j + 1), rdesc(j + 1));
           mma_commit_e(&s.s_full[0]);
         }
         // O1 += P1 V_j, then S1 of the next key tile
@@ -352,8 +376,8 @@ __global__ void __launch_bounds__(384, 1)
         // a latent key tile is also V_j: both PV products have read it
         if (LAT) mma_commit_e(&s.empty[sv]);
         if (more) {
-          issue_s<DQK, BN, C::ID_S>(tm + BN, qd1,
-                                    sdesc(smem_u32(s.ring[sk1]), 16, 1024));
+          issue_s<DQK, KC, BN, C::ID_S>(tm + BN, qd1, kdesc(j + 1),
+                                        rdesc(j + 1));
           mma_commit_e(&s.s_full[1]);
         }
       }
@@ -397,6 +421,10 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       tc_fence_after();
+      if (LAT && t == 1 && threadIdx.x == 256) {
+        // S1_j has run, and with it S0_j: both have read key tile j's r part
+        mbar_arrive(&s.r_empty[j % C::NSR]);
+      }
       if (!LAT && t == 1 && threadIdx.x == 256) {
         // S1_j has run, and with it every product issued before it: both
         // S products of K_j and both PV products of V_{j-1}
