@@ -86,7 +86,6 @@ struct __align__(1024) FwdSmem {
   __nv_bfloat16 ring[C::NS][BN * C::RING_COLS];
   __nv_bfloat16 rring[LAT ? C::NSR : 1][LAT ? BN * C::R_COLS : 64];
   uint64_t q_full;
-  uint64_t full[C::NS];
   uint64_t empty[C::NS];
   uint64_t r_empty[C::NSR];  // latent pages: the r slots
   // K/V pages: group 0 is K_0, group g > 0 is V_{g-1} and K_g (the ring
@@ -203,10 +202,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 1);
-    }
+    for (int i = 0; i < NS; ++i) mbar_init(&s.empty[i], 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s.s_full[t], 1);
       mbar_init(&s.p_full[t], 128);
